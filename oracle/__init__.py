@@ -1,0 +1,148 @@
+"""fp64 CPU oracle for the DSA hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg may import this package.  The product library never calls it
+and shares no code with it: the arithmetic lives in ``oracle.c`` (plain C,
+OpenMP over query rows), compiled here with gcc into ``_build/liboracle.so``.
+
+Functions (all take numpy arrays; bf16 tensors as uint16 bit patterns):
+  indexer_scores(batch, rows)          -> float64 [len(rows), ld]
+  topk(batch, scores_f32, rows, k)     -> int32   [len(rows), k]
+  sparse_mla(batch, idx, rows)         -> (float64 [n, 64, 512], float64 [n, 64])
+  masked_mla(batch, idx, rows)         -> same, written in the pages' mask form
+See ``oracle.c`` for what each computes and the passages it follows.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+H_IDX, D_IDX, H, D_QK, D_V = 32, 128, 64, 576, 512
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (-O2, OpenMP, no fast-math, no contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            lib.oracle_indexer_scores.argtypes = [i32, P, P, i64, P, P, P, i32, P, P, i64]
+            lib.oracle_topk.argtypes = [i32, P, P, P, i64, i32, P, i32, P]
+            lib.oracle_sparse_mla.argtypes = [i32, P, P, i64, P, P, P, i32, dbl, i32, P, P, P]
+            lib.oracle_masked_mla.argtypes = [i32, P, P, i64, P, P, P, i32, dbl, i32, P, P, P]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _np(x, dtype) -> np.ndarray:
+    if hasattr(x, "detach"):          # a torch tensor (CPU copy is taken)
+        x = x.detach().cpu()
+        if str(x.dtype) == "torch.bfloat16":
+            import torch
+            x = x.view(torch.int16)
+        x = x.numpy()
+    a = np.asarray(x)
+    if a.dtype != dtype:
+        if dtype == np.uint16 and a.dtype == np.int16:
+            a = a.view(np.uint16)          # bf16 bit patterns
+        else:
+            a = a.astype(dtype)
+    return np.ascontiguousarray(a)
+
+
+def _rows(batch, rows: Optional[Sequence[int]]) -> np.ndarray:
+    if rows is None:
+        rows = range(batch.total_q)
+    return np.ascontiguousarray(np.asarray(list(rows), dtype=np.int32))
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def indexer_scores(batch, rows: Optional[Sequence[int]] = None, ld: Optional[int] = None) -> np.ndarray:
+    """Lightning-indexer scores; entries s > t of each row are NaN."""
+    lib = _load()
+    r = _rows(batch, rows)
+    ld = int(ld if ld is not None else max(batch.max_ctx, 1))
+    out = np.full((len(r), ld), np.nan, dtype=np.float64)
+    q_off, ctx = _np(batch.q_off, np.int32), _np(batch.ctx_len, np.int32)
+    qi, w, ki = _np(batch.q_idx, np.uint16), _np(batch.w, np.float32), _np(batch.k_idx, np.uint16)
+    lib.oracle_indexer_scores(batch.B, _ptr(q_off), _ptr(ctx), int(batch.stride), _ptr(qi), _ptr(w),
+                              _ptr(ki), len(r), _ptr(r), _ptr(out), ld)
+    return out
+
+
+def topk(batch, scores: np.ndarray, rows: Optional[Sequence[int]] = None, k: Optional[int] = None) -> np.ndarray:
+    """Causal top-k of fp32 score rows (row j of ``scores`` belongs to rows[j])."""
+    lib = _load()
+    r = _rows(batch, rows)
+    k = int(k if k is not None else batch.k)
+    s = np.ascontiguousarray(np.asarray(scores, dtype=np.float32))
+    assert s.ndim == 2 and s.shape[0] == len(r)
+    out = np.empty((len(r), k), dtype=np.int32)
+    q_off, ctx = _np(batch.q_off, np.int32), _np(batch.ctx_len, np.int32)
+    lib.oracle_topk(batch.B, _ptr(q_off), _ptr(ctx), _ptr(s), s.shape[1], len(r), _ptr(r), k, _ptr(out))
+    return out
+
+
+def _mla(fn, batch, idx, rows, sm_scale) -> Tuple[np.ndarray, np.ndarray]:
+    r = _rows(batch, rows)
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int32))
+    assert idx.ndim == 2 and idx.shape[0] == len(r)
+    k = idx.shape[1]
+    out = np.empty((len(r), H, D_V), dtype=np.float64)
+    lse = np.empty((len(r), H), dtype=np.float64)
+    q_off, ctx = _np(batch.q_off, np.int32), _np(batch.ctx_len, np.int32)
+    q, kv = _np(batch.q, np.uint16), _np(batch.kv, np.uint16)
+    scale = float(sm_scale if sm_scale is not None else batch.sm_scale)
+    fn(batch.B, _ptr(q_off), _ptr(ctx), int(batch.stride), _ptr(q), _ptr(kv), _ptr(idx), k, scale,
+       len(r), _ptr(r), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def sparse_mla(batch, idx, rows=None, sm_scale=None):
+    """Absorbed-form attention over the selected latent rows (gather form)."""
+    return _mla(_load().oracle_sparse_mla, batch, idx, rows, sm_scale)
+
+
+def masked_mla(batch, idx, rows=None, sm_scale=None):
+    """The same attention in the pages' dense-mask form."""
+    return _mla(_load().oracle_masked_mla, batch, idx, rows, sm_scale)

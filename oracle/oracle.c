@@ -1,0 +1,252 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU oracle for the DSA hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg call this library.  It shares no code,
+ * header, table or helper with the CUDA library: every input arrives as a
+ * raw array (bf16 as its 16-bit pattern, widened here exactly).
+ *
+ * What it computes, and where the pages define it:
+ *
+ *  oracle_indexer_scores  -- lightning-indexer score of query position t
+ *      against every causal history position s <= t,
+ *          I[t,s] = sum_h w[t,h] * ReLU( sum_d q_idx[t,h,d] * k_idx[s,d] ),
+ *      32 heads x 128 dims, one shared 128-dim key per token, arithmetic in
+ *      floating point wider than the bf16 inputs ("GLM-5.1 架构深度拆解",
+ *      section 3.2 "Indexer 公式" Steps 4-5 and section 3.6 Step 5: two
+ *      einsums in fp32 with a ReLU between them; the GLM-5 explainer page,
+ *      indexer paragraph).  Any positive softmax_scale of the pages factors
+ *      out of the ReLU and is taken to be folded into w.
+ *  oracle_topk            -- causal top-k of one fp32 score row
+ *      (section 3.6 Steps 6-7: mask s > t, keep min(index_topk, length);
+ *      explainer page: "shorter than 2048 keeps all"; section 3.4: the
+ *      top-k must be deterministic).  Reading used here: ties are broken
+ *      toward the lower position, -0.0 equals +0.0, the chosen positions
+ *      are emitted in ascending order and the tail is padded with -1.
+ *  oracle_sparse_mla      -- attention of one query's 64 heads over the
+ *      selected rows of the latent cache in absorbed form: logits
+ *      sm_scale * q[h] . kv[s] over all 576 columns (512 latent + 64 RoPE
+ *      key shared by every head), softmax over the selected rows, output
+ *      the softmax-weighted sum of the first 512 columns (section 3.1
+ *      "DSA 原理" step 2, section 4.2 shared single-head RoPE key, section
+ *      2.5 576-wide cached row; explainer page: the top-2048 ids only
+ *      drive the gather).  Also returns lse = m + log(sum exp(l - m)).
+ *  oracle_masked_mla      -- the same attention written the way the pages'
+ *      attention layer does it (section 4.5 Steps 6-7): a dense row of
+ *      -inf with 0 scattered at the selected positions, plus the causal
+ *      mask, added to the logits of *every* cached position before the
+ *      softmax.  Used to check the gather form against the mask form.
+ *
+ * Plain loops, no blocking, no reordering; OpenMP only splits query rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { O_HIDX = 32, O_DIDX = 128, O_H = 64, O_DQK = 576, O_DV = 512 };
+
+static double widen_bf16(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* sequence b and position t of packed query row r */
+static void locate_row(int B, const int32_t* q_off, const int32_t* ctx_len, int32_t r,
+                       int* b_out, int64_t* t_out) {
+    int b = 0;
+    while (b + 1 < B && q_off[b + 1] <= r) b++;
+    int64_t nq = (int64_t)q_off[b + 1] - q_off[b];
+    *b_out = b;
+    *t_out = (int64_t)ctx_len[b] - nq + ((int64_t)r - q_off[b]);
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* out[j*ld + s] = I[t,s] for s in [0, t] of requested row rows[j]; other
+ * entries of the row are left untouched. */
+void oracle_indexer_scores(int B, const int32_t* q_off, const int32_t* ctx_len, int64_t stride,
+                           const uint16_t* q_idx, const float* w, const uint16_t* k_idx,
+                           int nrows, const int32_t* rows, double* out, int64_t ld) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int j = 0; j < nrows; j++) {
+        int b;
+        int64_t t;
+        locate_row(B, q_off, ctx_len, rows[j], &b, &t);
+        const uint16_t* qr = q_idx + (int64_t)rows[j] * O_HIDX * O_DIDX;
+        const float* wr = w + (int64_t)rows[j] * O_HIDX;
+        for (int64_t s = 0; s <= t; s++) {
+            const uint16_t* ks = k_idx + ((int64_t)b * stride + s) * O_DIDX;
+            double score = 0.0;
+            for (int h = 0; h < O_HIDX; h++) {
+                double dot = 0.0;
+                for (int d = 0; d < O_DIDX; d++)
+                    dot += widen_bf16(qr[h * O_DIDX + d]) * widen_bf16(ks[d]);
+                double relu = dot > 0.0 ? dot : 0.0;
+                score += (double)wr[h] * relu;
+            }
+            out[(int64_t)j * ld + s] = score;
+        }
+    }
+}
+
+typedef struct {
+    float v;
+    int32_t s;
+} cand_t;
+
+/* larger score first; equal scores (-0.0 == +0.0) -> lower position first */
+static int by_score_then_pos(const void* pa, const void* pb) {
+    const cand_t* a = (const cand_t*)pa;
+    const cand_t* b = (const cand_t*)pb;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->s > b->s) - (a->s < b->s);
+}
+
+static int by_pos(const void* pa, const void* pb) {
+    int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+    return (a > b) - (a < b);
+}
+
+/* idx_out[j*k + i]: for requested row rows[j] (position t) the min(k, t+1)
+ * positions with the largest scores[j*ld + s], s <= t, ascending, then -1. */
+void oracle_topk(int B, const int32_t* q_off, const int32_t* ctx_len,
+                 const float* scores, int64_t ld, int nrows, const int32_t* rows, int k,
+                 int32_t* idx_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int j = 0; j < nrows; j++) {
+        int b;
+        int64_t t;
+        locate_row(B, q_off, ctx_len, rows[j], &b, &t);
+        int64_t n = t + 1;
+        int64_t m = n < k ? n : k;
+        cand_t* c = (cand_t*)malloc((size_t)(n > 0 ? n : 1) * sizeof(cand_t));
+        for (int64_t s = 0; s < n; s++) {
+            c[s].v = scores[(int64_t)j * ld + s];
+            c[s].s = (int32_t)s;
+        }
+        qsort(c, (size_t)n, sizeof(cand_t), by_score_then_pos);
+        int32_t* o = idx_out + (int64_t)j * k;
+        for (int64_t i = 0; i < m; i++) o[i] = c[i].s;
+        qsort(o, (size_t)m, sizeof(int32_t), by_pos);
+        for (int64_t i = m; i < k; i++) o[i] = -1;
+        free(c);
+    }
+}
+
+/* out[j, h, 0:512], lse[j, h] for requested row rows[j], attending over the
+ * positions idx[j*k + i] >= 0. */
+void oracle_sparse_mla(int B, const int32_t* q_off, const int32_t* ctx_len, int64_t stride,
+                       const uint16_t* q, const uint16_t* kv, const int32_t* idx, int k,
+                       double sm_scale, int nrows, const int32_t* rows, double* out,
+                       double* lse) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int j = 0; j < nrows; j++) {
+        int b;
+        int64_t t;
+        locate_row(B, q_off, ctx_len, rows[j], &b, &t);
+        const int32_t* sel = idx + (int64_t)j * k;
+        double* logit = (double*)malloc((size_t)k * sizeof(double));
+        for (int h = 0; h < O_H; h++) {
+            const uint16_t* qh = q + ((int64_t)rows[j] * O_H + h) * O_DQK;
+            double mx = -INFINITY;
+            for (int i = 0; i < k; i++) {
+                if (sel[i] < 0) continue;
+                const uint16_t* row = kv + ((int64_t)b * stride + sel[i]) * O_DQK;
+                double dot = 0.0;
+                for (int d = 0; d < O_DQK; d++) dot += widen_bf16(qh[d]) * widen_bf16(row[d]);
+                logit[i] = sm_scale * dot;
+                if (logit[i] > mx) mx = logit[i];
+            }
+            double* o = out + ((int64_t)j * O_H + h) * O_DV;
+            for (int d = 0; d < O_DV; d++) o[d] = 0.0;
+            double z = 0.0;
+            for (int i = 0; i < k; i++) {
+                if (sel[i] < 0) continue;
+                const uint16_t* row = kv + ((int64_t)b * stride + sel[i]) * O_DQK;
+                double p = exp(logit[i] - mx);
+                z += p;
+                for (int d = 0; d < O_DV; d++) o[d] += p * widen_bf16(row[d]);
+            }
+            if (z > 0.0) {
+                for (int d = 0; d < O_DV; d++) o[d] /= z;
+                lse[(int64_t)j * O_H + h] = mx + log(z);
+            } else {
+                lse[(int64_t)j * O_H + h] = -INFINITY;
+            }
+        }
+        free(logit);
+    }
+}
+
+/* The mask formulation: logits over every cached position s < ctx_len[b]
+ * plus index_mask[s] (0 where s is selected, -inf elsewhere) plus the
+ * causal mask (0 for s <= t, -inf for s > t); softmax over the whole row. */
+void oracle_masked_mla(int B, const int32_t* q_off, const int32_t* ctx_len, int64_t stride,
+                       const uint16_t* q, const uint16_t* kv, const int32_t* idx, int k,
+                       double sm_scale, int nrows, const int32_t* rows, double* out,
+                       double* lse) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int j = 0; j < nrows; j++) {
+        int b;
+        int64_t t;
+        locate_row(B, q_off, ctx_len, rows[j], &b, &t);
+        int64_t ctx = ctx_len[b];
+        double* index_mask = (double*)malloc((size_t)(ctx > 0 ? ctx : 1) * sizeof(double));
+        double* logit = (double*)malloc((size_t)(ctx > 0 ? ctx : 1) * sizeof(double));
+        for (int64_t s = 0; s < ctx; s++) index_mask[s] = -INFINITY;
+        for (int i = 0; i < k; i++)
+            if (idx[(int64_t)j * k + i] >= 0 && idx[(int64_t)j * k + i] < ctx)
+                index_mask[idx[(int64_t)j * k + i]] = 0.0;
+        for (int h = 0; h < O_H; h++) {
+            const uint16_t* qh = q + ((int64_t)rows[j] * O_H + h) * O_DQK;
+            double mx = -INFINITY;
+            for (int64_t s = 0; s < ctx; s++) {
+                const uint16_t* row = kv + ((int64_t)b * stride + s) * O_DQK;
+                double dot = 0.0;
+                for (int d = 0; d < O_DQK; d++) dot += widen_bf16(qh[d]) * widen_bf16(row[d]);
+                double causal = s <= t ? 0.0 : -INFINITY;
+                logit[s] = sm_scale * dot + index_mask[s] + causal;
+                if (logit[s] > mx) mx = logit[s];
+            }
+            double* o = out + ((int64_t)j * O_H + h) * O_DV;
+            for (int d = 0; d < O_DV; d++) o[d] = 0.0;
+            double z = 0.0;
+            for (int64_t s = 0; s < ctx; s++) {
+                double p = isinf(logit[s]) && logit[s] < 0 ? 0.0 : exp(logit[s] - mx);
+                if (p == 0.0) continue;
+                const uint16_t* row = kv + ((int64_t)b * stride + s) * O_DQK;
+                z += p;
+                for (int d = 0; d < O_DV; d++) o[d] += p * widen_bf16(row[d]);
+            }
+            if (z > 0.0) {
+                for (int d = 0; d < O_DV; d++) o[d] /= z;
+                lse[(int64_t)j * O_H + h] = mx + log(z);
+            } else {
+                lse[(int64_t)j * O_H + h] = -INFINITY;
+            }
+        }
+        free(index_mask);
+        free(logit);
+    }
+}
