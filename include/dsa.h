@@ -1,0 +1,161 @@
+/*
+ * dsa.h -- C ABI of libdsa.so: the GLM-5 DSA attention hot path on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The path has three steps, each an entry point below, plus one call that
+ * runs all three:
+ *
+ *   1. dsa_indexer_scores -- lightning indexer.  For query position t and
+ *      every causal history position s <= t
+ *          I[t,s] = sum_{h<32} w[t,h] * ReLU( sum_{d<128} q_idx[t,h,d] * k_idx[s,d] )
+ *      ("GLM-5.1 架构深度拆解", section 3.2 "Indexer 公式" Steps 4-5 and
+ *      section 3.6 Step 5; the GLM-5 explainer page: 32 index queries of
+ *      128 dims, one 128-dim index key per position, ReLU, 32 weights).
+ *      Products and sums are fp32 (the pages cast both operands to fp32).
+ *      Any positive softmax_scale factors out of the ReLU; fold it into w.
+ *   2. dsa_topk -- causal top-k (section 3.6 Steps 6-7: positions s > t are
+ *      masked, min(index_topk, length) positions are kept; section 3.4: the
+ *      selection must be deterministic; explainer page: a query that sees
+ *      fewer than 2048 positions keeps all of them).
+ *   3. dsa_sparse_mla_fwd -- 64-head softmax attention over the selected
+ *      rows of the latent cache, absorbed form: each cached row is
+ *      [512 latent || 64 RoPE key] (section 2.5, section 4.2: the RoPE key
+ *      is one stream shared by all heads), QK runs over all 576 columns and
+ *      V is the first 512 (explainer page: the top-2048 ids only drive the
+ *      gather; section 3.1 step 2: exact attention on the selected tokens).
+ *   4. dsa_forward -- 1 -> 2 -> 3 for prefill, chunked prefill and decode.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - bf16 tensors are passed as their 16-bit patterns (uint16_t).
+ *  - Every tensor pointer is a DEVICE pointer unless stated otherwise, and
+ *    must be 16-byte aligned.  The caller owns every buffer; the library
+ *    allocates nothing and keeps no pointer after a call returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    are stream-ordered and asynchronous; none synchronises except
+ *    dsa_read_device_status.  Calls on different streams that share a
+ *    workspace race.
+ *  - Query rows of all sequences are packed: row r of sequence b is
+ *    q_off[b] + i, i in [0, n_b), n_b = q_off[b+1] - q_off[b], and sits at
+ *    position t = ctx_len[b] - n_b + i.  The caches hold sequence b's
+ *    positions at rows b * cache_stride + s.  The caller appends the new
+ *    tokens' cache rows before the call (the pages append the new index key
+ *    before scoring it), so ctx_len counts them.
+ *  - Host-side argument errors return DSA_ERR_INVALID_ARG and launch
+ *    nothing.  Errors only the device can see (a q_off/ctx_len that breaks
+ *    the bounds below, an index outside [-1, t]) skip the offending row,
+ *    leave its outputs unwritten, and latch a code in the workspace's status
+ *    word, read back by dsa_read_device_status.  Kernels never trap.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#define DSA_INDEX_HEADS 32   /* index_n_heads */
+#define DSA_INDEX_DIM 128    /* index_head_dim */
+#define DSA_HEADS 64         /* num_attention_heads */
+#define DSA_QK_DIM 576       /* kv_lora_rank 512 + qk_rope_head_dim 64 */
+#define DSA_V_DIM 512        /* kv_lora_rank */
+#define DSA_MAX_TOPK 2048    /* index_topk */
+
+typedef enum dsa_status {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1, /* host-side argument check failed; nothing launched */
+    DSA_ERR_UNSUPPORTED = 2, /* a shape or mode this build does not implement */
+    DSA_ERR_WORKSPACE = 3,   /* ws is NULL or ws_bytes < dsa_workspace_size() */
+    DSA_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+    DSA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel expired */
+    DSA_ERR_BAD_BATCH = 6,   /* device: q_off / ctx_len outside the host bounds */
+    DSA_ERR_BAD_INDEX = 7    /* device: a selected index outside [-1, t] */
+} dsa_status;
+
+/* One call's batch.  q_off and ctx_len are DEVICE int32 arrays so that a
+ * captured launch sequence can be replayed with new lengths; the host only
+ * gives upper bounds, used to size grids.  Device-side requirements, checked
+ * by the kernels (DSA_ERR_BAD_BATCH): q_off[0] = 0, q_off[batch] = total_q,
+ * 0 <= n_b <= max_q, n_b <= ctx_len[b] <= max_ctx. */
+typedef struct dsa_batch {
+    int32_t batch;            /* B >= 1 sequences */
+    int32_t total_q;          /* packed query rows, >= 0 */
+    int32_t max_q;            /* bound on n_b */
+    int32_t max_ctx;          /* bound on ctx_len[b]; <= cache_stride */
+    int64_t cache_stride;     /* cache rows per sequence */
+    const int32_t* q_off;     /* device [B+1] */
+    const int32_t* ctx_len;   /* device [B] */
+} dsa_batch;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+DSA_API const char* dsa_status_string(int status);
+
+/* Bytes of workspace that every call below needs for `batch` and top-k `k`
+ * (the largest of them).  Host only; launches nothing. */
+DSA_API dsa_status dsa_workspace_size(const dsa_batch* batch, int k, size_t* bytes);
+
+/* Clears the device status word of a workspace (stream-ordered memset).
+ * A fresh workspace must be cleared once before its first use. */
+DSA_API dsa_status dsa_reset_device_status(void* ws, void* stream);
+
+/* Synchronises `stream`, then copies the workspace's status word to *out
+ * (DSA_OK if no kernel latched an error since the last reset). */
+DSA_API dsa_status dsa_read_device_status(const void* ws, void* stream, dsa_status* out);
+
+/* Step 1: lightning-indexer scores.
+ *   q_idx  bf16 [total_q, 32, 128]  post-RoPE index queries
+ *   w      fp32 [total_q, 32]       head weights
+ *   k_idx  bf16 [batch * cache_stride, 128]  index-key cache
+ *   scores fp32 [total_q, ld]       out: scores[r*ld + s] = I[t,s] for s <= t;
+ *                                   entries s > t are not written
+ * ld >= max_ctx, ld % 4 == 0.  Uses only the status word of ws. */
+DSA_API dsa_status dsa_indexer_scores(const dsa_batch* batch, const uint16_t* q_idx, const float* w,
+                              const uint16_t* k_idx, float* scores, int64_t ld, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* Step 2: causal top-k of score rows (as written by step 1).
+ *   idx int32 [total_q, k]  out: the min(k, t+1) positions s <= t with the
+ *       largest scores, ascending; entries past them are -1.  Scores are
+ *       compared as fp32 values (-0.0 == +0.0); of equal scores the lower
+ *       position wins.  Deterministic and bit-exact.  NaN scores are outside
+ *       the contract.
+ * 1 <= k <= 2048, ld >= max_ctx, ld % 4 == 0. */
+DSA_API dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t ld, int k, int32_t* idx,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* Step 3: sparse MLA attention, absorbed form.
+ *   q   bf16 [total_q, 64, 576]            absorbed queries
+ *   kv  bf16 [batch * cache_stride, 576]   latent cache ([512 latent || 64 rope])
+ *   idx int32 [total_q, k]                 selected positions, -1 = none
+ *   out bf16 [total_q, 64, 512]            softmax(sm_scale * q.kv) @ kv[:, :512]
+ *   lse fp32 [total_q, 64] or NULL         natural-log sum-exp of the logits
+ * A row with no valid index gets out = 0 and lse = -inf.  Entries outside
+ * [-1, t] latch DSA_ERR_BAD_INDEX and are skipped. */
+DSA_API dsa_status dsa_sparse_mla_fwd(const dsa_batch* batch, const uint16_t* q, const uint16_t* kv,
+                              const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 1-3 in one call (prefill, one chunk of a chunked prefill, or a
+ * decode step).  idx_out [total_q, k] and scores_out [total_q, ld] are
+ * optional (NULL = keep them in the workspace only); ld is ignored when
+ * scores_out is NULL.  Results equal steps 1-3 called one by one, bit for
+ * bit. */
+DSA_API dsa_status dsa_forward(const dsa_batch* batch, const uint16_t* q_idx, const float* w,
+                       const uint16_t* k_idx, const uint16_t* q, const uint16_t* kv, int k,
+                       float sm_scale, uint16_t* out, float* lse, int32_t* idx_out,
+                       float* scores_out, int64_t ld, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

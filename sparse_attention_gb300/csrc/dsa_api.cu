@@ -1,0 +1,206 @@
+// dsa_api.cu -- the extern "C" entry points of libdsa.so (declared and
+// documented in include/dsa.h): host-side argument checks, workspace
+// layout, and the launch sequence of dsa_forward.
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+
+#include "internal.h"
+
+namespace dsa {
+namespace {
+
+// Scores of one dsa_forward chunk are sized to stay resident in the 126 MB
+// L2 between the indexer that writes them and the top-k that reads them.
+constexpr size_t kScoreChunkBytes = size_t(64) << 20;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+dsa_status check_batch(const dsa_batch* b) {
+    if (!b) return DSA_ERR_INVALID_ARG;
+    if (b->batch < 1 || b->batch > 65535) return DSA_ERR_INVALID_ARG;
+    if (b->total_q < 0 || b->max_q < 0 || b->max_ctx < 0) return DSA_ERR_INVALID_ARG;
+    if (b->max_q > (1 << 19)) return DSA_ERR_UNSUPPORTED;            // grid limits
+    if (b->total_q >= (1 << 26)) return DSA_ERR_UNSUPPORTED;         // TMA row coordinates
+    if (b->cache_stride < b->max_ctx || b->cache_stride < 0) return DSA_ERR_INVALID_ARG;
+    if ((int64_t)b->batch * b->cache_stride >= (int64_t(1) << 31)) return DSA_ERR_UNSUPPORTED;
+    if (!b->q_off || !b->ctx_len) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+BatchDev to_dev(const dsa_batch* b) {
+    return BatchDev{b->batch, b->total_q, b->max_q, b->max_ctx, b->cache_stride, b->q_off, b->ctx_len};
+}
+
+struct WsLayout {
+    int32_t chunk_rows;     // local query rows per dsa_forward chunk
+    int64_t ld_s;           // row stride of the scratch score rows
+    size_t off_scores, off_idx, off_attn, attn_bytes, total;
+};
+
+WsLayout ws_layout(const dsa_batch* b, int k) {
+    WsLayout L{};
+    const BatchDev bd = to_dev(b);
+    L.ld_s = std::max<int64_t>(4, ((int64_t)b->max_ctx + 3) / 4 * 4);
+    const size_t row_bytes = (size_t)b->batch * L.ld_s * sizeof(float);
+    int64_t rows = (int64_t)(kScoreChunkBytes / std::max<size_t>(row_bytes, 1));
+    rows = std::max<int64_t>(1, std::min<int64_t>(rows, std::max(b->max_q, 1)));
+    L.chunk_rows = (int32_t)rows;
+    size_t off = kWsHeaderBytes;
+    L.off_scores = off;
+    off = round_up(off + (size_t)b->batch * rows * L.ld_s * sizeof(float), 256);
+    L.off_idx = off;
+    off = round_up(off + (size_t)b->batch * rows * k * sizeof(int32_t), 256);
+    L.off_attn = off;
+    // attention scratch for a forward chunk or for a whole-batch call
+    L.attn_bytes = std::max(sparse_mla_scratch_bytes(bd, rows, k), sparse_mla_scratch_bytes(bd, b->max_q, k));
+    off = round_up(off + L.attn_bytes, 256);
+    L.total = off;
+    return L;
+}
+
+dsa_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DSA_OK;
+    cudaGetLastError();  // clear a sticky launch error of this thread
+    return DSA_ERR_CUDA;
+}
+
+dsa_status check_ws(const dsa_batch* b, int k, void* ws, size_t ws_bytes) {
+    if (!ws || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(b, k).total) return DSA_ERR_WORKSPACE;
+    return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+const char* dsa_status_string(int s) {
+    switch (s) {
+        case DSA_OK: return "DSA_OK";
+        case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG: an argument failed the host-side check";
+        case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED: shape or mode not implemented";
+        case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case DSA_ERR_CUDA: return "DSA_ERR_CUDA: a CUDA launch or runtime call failed";
+        case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: a bounded in-kernel wait expired";
+        case DSA_ERR_BAD_BATCH: return "DSA_ERR_BAD_BATCH: q_off/ctx_len outside the host bounds";
+        case DSA_ERR_BAD_INDEX: return "DSA_ERR_BAD_INDEX: a selected index outside [-1, t]";
+        default: return "unknown dsa_status";
+    }
+}
+
+dsa_status dsa_workspace_size(const dsa_batch* batch, int k, size_t* bytes) {
+    if (!bytes) return DSA_ERR_INVALID_ARG;
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+    *bytes = ws_layout(batch, k).total;
+    return DSA_OK;
+}
+
+dsa_status dsa_reset_device_status(void* ws, void* stream) {
+    if (!ws || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(ws, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_read_device_status(const void* ws, void* stream, dsa_status* out) {
+    if (!ws || !out) return DSA_ERR_INVALID_ARG;
+    int32_t v = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
+    *out = static_cast<dsa_status>(v);
+    return DSA_OK;
+}
+
+dsa_status dsa_indexer_scores(const dsa_batch* batch, const uint16_t* q_idx, const float* w, const uint16_t* k_idx,
+                              float* scores, int64_t ld, void* ws, size_t ws_bytes, void* stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (!ws || !aligned16(ws) || ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
+    if (batch->total_q == 0 || batch->max_q == 0) return DSA_OK;
+    if (!q_idx || !w || !k_idx || !scores) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(scores)) return DSA_ERR_INVALID_ARG;
+    if (ld < batch->max_ctx || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
+    const BatchDev bd = to_dev(batch);
+    return cuda_status(launch_indexer(bd, RowRange{0, batch->max_q}, q_idx, w, k_idx, scores, ld, false,
+                                      static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t ld, int k, int32_t* idx, void* ws,
+                    size_t ws_bytes, void* stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws) || ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
+    if (batch->total_q == 0 || batch->max_q == 0) return DSA_OK;
+    if (!scores || !idx || !aligned16(scores) || !aligned16(idx)) return DSA_ERR_INVALID_ARG;
+    if (ld < batch->max_ctx || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
+    const BatchDev bd = to_dev(batch);
+    return cuda_status(launch_topk(bd, RowRange{0, batch->max_q}, scores, ld, false, k, idx, false,
+                                   static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_sparse_mla_fwd(const dsa_batch* batch, const uint16_t* q, const uint16_t* kv, const int32_t* idx,
+                              int k, float sm_scale, uint16_t* out, float* lse, void* ws, size_t ws_bytes,
+                              void* stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+    if ((st = check_ws(batch, k, ws, ws_bytes)) != DSA_OK) return st;
+    if (batch->total_q == 0 || batch->max_q == 0) return DSA_OK;
+    if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(idx) || !aligned16(out) || (lse && !aligned16(lse)))
+        return DSA_ERR_INVALID_ARG;
+    if (!(sm_scale > 0.f) || sm_scale == INFINITY) return DSA_ERR_INVALID_ARG;
+    const BatchDev bd = to_dev(batch);
+    const WsLayout L = ws_layout(batch, k);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    return cuda_status(launch_sparse_mla(bd, RowRange{0, batch->max_q}, q, kv, idx, false, k, sm_scale, out, lse,
+                                         base + L.off_attn, L.attn_bytes, static_cast<int32_t*>(ws),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_forward(const dsa_batch* batch, const uint16_t* q_idx, const float* w, const uint16_t* k_idx,
+                       const uint16_t* q, const uint16_t* kv, int k, float sm_scale, uint16_t* out, float* lse,
+                       int32_t* idx_out, float* scores_out, int64_t ld, void* ws, size_t ws_bytes, void* stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+    if ((st = check_ws(batch, k, ws, ws_bytes)) != DSA_OK) return st;
+    if (batch->total_q == 0 || batch->max_q == 0) return DSA_OK;
+    if (!q_idx || !w || !k_idx || !q || !kv || !out) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q) || !aligned16(kv) ||
+        !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)) ||
+        (scores_out && !aligned16(scores_out)))
+        return DSA_ERR_INVALID_ARG;
+    if (scores_out && (ld < batch->max_ctx || ld % 4 != 0)) return DSA_ERR_INVALID_ARG;
+    if (!(sm_scale > 0.f) || sm_scale == INFINITY) return DSA_ERR_INVALID_ARG;
+
+    const BatchDev bd = to_dev(batch);
+    const WsLayout L = ws_layout(batch, k);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int32_t* status = static_cast<int32_t*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* sc = scores_out ? scores_out : reinterpret_cast<float*>(base + L.off_scores);
+    const int64_t sc_ld = scores_out ? ld : L.ld_s;
+    int32_t* ix = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + L.off_idx);
+    for (int32_t i0 = 0; i0 < batch->max_q; i0 += L.chunk_rows) {
+        const RowRange rr{i0, std::min(i0 + L.chunk_rows, batch->max_q)};
+        cudaError_t e = launch_indexer(bd, rr, q_idx, w, k_idx, sc, sc_ld, scores_out == nullptr, status, s);
+        if (e == cudaSuccess)
+            e = launch_topk(bd, rr, sc, sc_ld, scores_out == nullptr, k, ix, idx_out == nullptr, status, s);
+        if (e == cudaSuccess)
+            e = launch_sparse_mla(bd, rr, q, kv, ix, idx_out == nullptr, k, sm_scale, out, lse, base + L.off_attn,
+                                  L.attn_bytes, status, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return DSA_OK;
+}
+
+}  // extern "C"

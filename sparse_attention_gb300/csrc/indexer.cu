@@ -1,0 +1,308 @@
+// indexer.cu -- lightning-indexer scores on the 5th-generation tensor cores.
+//
+//   I[t,s] = sum_{h<32} w[t,h] * ReLU( q_idx[t,h,:] . k_idx[s,:] )
+//
+// ("GLM-5.1 架构深度拆解", section 3.2 Steps 4-5 and section 3.6 Step 5;
+// the GLM-5 explainer page, indexer paragraph.)
+//
+// The contraction over the 128 index dims is a dense GEMM: keys are the M
+// side (128 keys per tile, one TMEM lane per key) and a group of NQ
+// consecutive queries of one sequence times their 32 heads is the N side
+// (N = 32 * NQ).  One CTA owns one query group and a contiguous range of
+// key tiles; roles are split by warp:
+//   warp 0      TMA producer: the query block once, then key tiles through
+//               a ring of shared-memory stages (128B-swizzled boxes)
+//   warp 1      TMEM allocator and MMA issuer (tcgen05.mma kind::f16,
+//               bf16 x bf16 -> fp32), double-buffered accumulators
+//   warps 2..5  epilogue: tcgen05.ld one key row per thread, then the ReLU
+//               and the head-weighted sum in registers (fp32, heads in
+//               order), and a coalesced store of one fp32 score per
+//               (query, key) with s <= t.
+// Scores of positions s > t are never written.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstdio>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+template <int NQ>
+struct IdxCfg {
+    static constexpr int kN = NQ * kHIdx;            // MMA N: queries x heads
+    static constexpr int kBM = 128;                  // keys per tile: MMA M
+    static constexpr int kStages = (NQ == 1) ? 3 : 4;
+    static constexpr int kABoxBytes = kBM * 64 * 2;  // 64 of the 128 dims, 16 KiB
+    static constexpr int kABytes = 2 * kABoxBytes;
+    static constexpr int kBBoxBytes = kN * 64 * 2;
+    static constexpr int kBBytes = 2 * kBBoxBytes;
+    static constexpr int kAcc = 2;                   // TMEM accumulator buffers
+    static constexpr int kTmemCols = (kN * kAcc < 32) ? 32 : kN * kAcc;
+    static constexpr int kThreads = 192;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kABytes;
+    static constexpr int kOffW = kOffB + kBBytes;
+    static constexpr int kOffBar = kOffW + NQ * kHIdx * 4;
+    static constexpr int kNumBars = 2 * kStages + 1 + 2 * kAcc + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1 KiB alignment
+    static_assert(kTmemCols == 32 || kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 ||
+                      kTmemCols == 512,
+                  "TMEM allocation must be a power of two >= 32");
+    static_assert(kN % 16 == 0 && kN >= 16 && kN <= 256, "invalid MMA N for M = 128");
+};
+
+template <int NQ>
+__global__ void __launch_bounds__(192, 1)
+    indexer_kernel(const BatchDev bd, const RowRange rr, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_q, const float* __restrict__ w,
+                   float* __restrict__ scores, const int64_t ld, const int scores_local,
+                   const int tiles_per_split, int32_t* status) {
+    using C = IdxCfg<NQ>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int b = blockIdx.z;
+    SeqInfo sq;
+    if (!load_seq(bd, b, status, sq)) return;
+    const int32_t qlo = rr.i0 + (int32_t)blockIdx.y * NQ;           // local query indices [qlo, qhi)
+    const int32_t qhi = min(min(qlo + NQ, rr.i1), sq.nq);
+    if (qlo >= qhi) return;
+    const int32_t pos0 = sq.ctx - sq.nq;                             // position of local query 0
+    const int32_t ntiles = (pos0 + qhi - 1) / C::kBM + 1;
+    const int32_t j0 = (int32_t)blockIdx.x * tiles_per_split;
+    const int32_t j1 = min(j0 + tiles_per_split, ntiles);
+    if (j0 >= j1) return;
+    const int niter = j1 - j0;
+
+    const uint32_t sA = smem_u32(smem + C::kOffA);
+    const uint32_t sB = smem_u32(smem + C::kOffB);
+    float* w_s = reinterpret_cast<float*>(smem + C::kOffW);
+    const uint32_t bar0 = smem_u32(smem + C::kOffBar);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
+    const uint32_t bfull_bar = bar0 + 8u * (2 * C::kStages);
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::kStages + 1 + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::kStages + 1 + C::kAcc + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 1 + 2 * C::kAcc);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
+
+    const uint32_t warp = warp_id(), lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(bfull_bar, 1);
+        for (int a = 0; a < C::kAcc; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 128);
+        }
+        mbar_init(drain_bar, 1);
+        misc[1] = 0;  // abort flag
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(smem + C::kOffMisc), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp >= 2) {
+        // head weights of the group (0 for rows past the group's end)
+        for (int e = threadIdx.x - 64; e < NQ * kHIdx; e += 128) {
+            const int qi = e / kHIdx;
+            w_s[e] = (qlo + qi < qhi) ? __ldg(w + ((int64_t)sq.q0 + qlo + qi) * kHIdx + (e % kHIdx)) : 0.f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = misc[0];
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (elect_one()) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_q);
+            const int32_t qrow = (sq.q0 + qlo) * kHIdx;
+            mbar_arrive_expect_tx(bfull_bar, C::kBBytes);
+            tma_load_2d(sB, &tm_q, bfull_bar, 0, qrow);
+            tma_load_2d(sB + C::kBBoxBytes, &tm_q, bfull_bar, 64, qrow);
+            int issued = 0;
+            for (int it = 0; it < niter; ++it) {
+                const int s = it % C::kStages;
+                const uint32_t ph = (it / C::kStages) & 1u;
+                if (misc[1] || !mbar_wait(empty_bar(s), ph ^ 1u)) {
+                    latch_status(status, DSA_ERR_TIMEOUT);
+                    misc[1] = 1;
+                    break;
+                }
+                const int32_t krow = (int32_t)((int64_t)b * bd.stride + (int64_t)(j0 + it) * C::kBM);
+                mbar_arrive_expect_tx(full_bar(s), C::kABytes);
+                tma_load_2d(sA + s * C::kABytes, &tm_k, full_bar(s), 0, krow);
+                tma_load_2d(sA + s * C::kABytes + C::kABoxBytes, &tm_k, full_bar(s), 64, krow);
+                ++issued;
+            }
+            if (misc[1]) {
+                // wind down: let every copy this thread started land first
+                for (int it = max(0, issued - C::kStages); it < issued; ++it)
+                    mbar_wait(full_bar(it % C::kStages), (it / C::kStages) & 1u);
+                mbar_wait(bfull_bar, 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (elect_one()) {
+            constexpr uint32_t idesc = idesc_bf16_f32(C::kBM, C::kN);
+            bool ok = mbar_wait(bfull_bar, 0);
+            tc_fence_after();
+            for (int it = 0; ok && it < niter; ++it) {
+                const int s = it % C::kStages;
+                const int a = it & 1;
+                if (misc[1] || !mbar_wait(full_bar(s), (it / C::kStages) & 1u) ||
+                    !mbar_wait(tempty_bar(a), ((it >> 1) & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(a * C::kN);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ad =
+                            sdesc_sw128(sA + s * C::kABytes + kb * C::kABoxBytes + ks * 32, 16, 1024);
+                        const uint64_t bdsc = sdesc_sw128(sB + kb * C::kBBoxBytes + ks * 32, 16, 1024);
+                        mma_bf16_ss(d, ad, bdsc, idesc, (kb | ks) != 0);
+                    }
+                }
+                mma_commit(empty_bar(s));
+                mma_commit(tfull_bar(a));
+            }
+            if (!ok) {
+                latch_status(status, DSA_ERR_TIMEOUT);
+                misc[1] = 1;
+            }
+            // every MMA this thread issued has finished once drain completes
+            mma_commit(drain_bar);
+            mbar_wait(drain_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- epilogue
+        const uint32_t lq = warp & 3u;                     // TMEM lane quarter of this warp
+        const int32_t row = (int32_t)(lq * 32 + lane);     // key row within the tile
+        for (int it = 0; it < niter; ++it) {
+            const int a = it & 1;
+            bool ok = !misc[1] && mbar_wait(tfull_bar(a), (it >> 1) & 1u);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                latch_status(status, DSA_ERR_TIMEOUT);
+                misc[1] = 1;
+                break;
+            }
+            tc_fence_after();
+            const int32_t s = (j0 + it) * C::kBM + row;
+#pragma unroll 1
+            for (int qi = 0; qi < NQ; ++qi) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + ((lq * 32u) << 16) + (uint32_t)(a * C::kN + qi * 32), r);
+                tmem_ld_wait();
+                const int32_t i = qlo + qi;
+                if (i < qhi) {
+                    const float* wq = w_s + qi * kHIdx;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int h = 0; h < kHIdx; ++h) acc = fmaf(wq[h], fmaxf(__uint_as_float(r[h]), 0.f), acc);
+                    if (s <= pos0 + i) scores[buf_row(scores_local, sq, b, i, rr) * ld + s] = acc;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(a));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, 128] with 256-byte rows, 128B swizzle, box {64, box_rows}.
+bool make_tmap_bf16_128(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NQ>
+cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, const float* w,
+                      const uint16_t* k_idx, float* scores, int64_t ld, bool scores_local, int32_t* status,
+                      cudaStream_t stream) {
+    using C = IdxCfg<NQ>;
+    const int32_t rows_per_seq = min(rr.i1, bd.max_q) - rr.i0;
+    if (rows_per_seq <= 0 || bd.max_ctx <= 0) return cudaSuccess;
+    const int32_t groups = (rows_per_seq + NQ - 1) / NQ;
+    const int32_t tiles = (bd.max_ctx + C::kBM - 1) / C::kBM;
+    int tps;
+    if (NQ > 1) {
+        tps = 16;
+    } else {
+        // decode-like: spread every sequence's key stream over enough CTAs
+        // for ~4 CTAs per SM in total
+        const int64_t total = (int64_t)tiles * groups * bd.B;
+        tps = (int)std::max<int64_t>(4, (total + 4 * kNumSMs - 1) / (4 * kNumSMs));
+    }
+    const int32_t splits = (tiles + tps - 1) / tps;
+    CUtensorMap tm_k, tm_q;
+    if (!make_tmap_bf16_128(&tm_k, k_idx, (uint64_t)bd.B * (uint64_t)bd.stride, C::kBM)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_128(&tm_q, q_idx, (uint64_t)bd.total_q * kHIdx, C::kN)) return cudaErrorInvalidValue;
+    cudaError_t e =
+        cudaFuncSetAttribute(indexer_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(splits, groups, bd.B);
+    indexer_kernel<NQ><<<grid, C::kThreads, C::kSmemBytes, stream>>>(bd, rr, tm_k, tm_q, w, scores, ld,
+                                                                      scores_local ? 1 : 0, tps, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, const float* w,
+                           const uint16_t* k_idx, float* scores, int64_t ld, bool scores_local,
+                           int32_t* status, cudaStream_t stream) {
+    if (bd.max_q >= 16)
+        return launch_nq<8>(bd, rr, q_idx, w, k_idx, scores, ld, scores_local, status, stream);
+    return launch_nq<1>(bd, rr, q_idx, w, k_idx, scores, ld, scores_local, status, stream);
+}
+
+}  // namespace dsa

@@ -1,0 +1,86 @@
+// internal.h -- definitions shared by the CUDA translation units of libdsa.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+constexpr int kHIdx = DSA_INDEX_HEADS;   // 32 indexer heads
+constexpr int kDIdx = DSA_INDEX_DIM;     // 128 dims per indexer head / key
+constexpr int kH = DSA_HEADS;            // 64 attention heads
+constexpr int kDQK = DSA_QK_DIM;         // 576 = 512 latent + 64 rope
+constexpr int kDV = DSA_V_DIM;           // 512
+constexpr int kMaxTopk = DSA_MAX_TOPK;   // 2048
+constexpr int kNumSMs = 152;             // GB300
+
+// Upper bound on any single in-kernel wait (a phase of an mbarrier).  A wait
+// that exceeds it latches DSA_ERR_TIMEOUT and the kernel winds down.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// The first 256 bytes of every workspace: the device status word.
+constexpr size_t kWsHeaderBytes = 256;
+
+// Device view of dsa_batch.
+struct BatchDev {
+    int32_t B, total_q, max_q, max_ctx;
+    int64_t stride;
+    const int32_t* q_off;
+    const int32_t* ctx_len;
+};
+
+// The local query indices [i0, i1) of every sequence that one launch
+// processes.  A per-row buffer is either addressed by the packed row
+// q_off[b] + i ("global") or, for chunk-sized scratch, by
+// b * (i1 - i0) + (i - i0) ("local").
+struct RowRange {
+    int32_t i0, i1;
+};
+
+struct SeqInfo {
+    int32_t q0, nq, ctx;
+};
+
+__device__ __forceinline__ void latch_status(int32_t* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// Loads and checks sequence b; false (and a latched DSA_ERR_BAD_BATCH) if
+// its q_off / ctx_len break the host bounds.
+__device__ __forceinline__ bool load_seq(const BatchDev& bd, int b, int32_t* status, SeqInfo& s) {
+    s.q0 = __ldg(bd.q_off + b);
+    const int32_t q1 = __ldg(bd.q_off + b + 1);
+    s.nq = q1 - s.q0;
+    s.ctx = __ldg(bd.ctx_len + b);
+    const bool ok = s.q0 >= 0 && q1 <= bd.total_q && s.nq >= 0 && s.nq <= bd.max_q && s.nq <= s.ctx &&
+                    s.ctx <= bd.max_ctx;
+    if (!ok) latch_status(status, DSA_ERR_BAD_BATCH);
+    return ok;
+}
+
+__device__ __forceinline__ int64_t buf_row(bool local, const SeqInfo& s, int b, int32_t i, RowRange rr) {
+    return local ? (int64_t)b * (rr.i1 - rr.i0) + (i - rr.i0) : (int64_t)s.q0 + i;
+}
+
+// ------------------------------------------------------------ launchers --
+
+cudaError_t launch_indexer(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, const float* w,
+                           const uint16_t* k_idx, float* scores, int64_t ld, bool scores_local,
+                           int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, int64_t ld,
+                        bool scores_local, int k, int32_t* idx, bool idx_local, int32_t* status,
+                        cudaStream_t stream);
+
+// Bytes of scratch the attention launch needs for `rows` query rows.
+size_t sparse_mla_scratch_bytes(const BatchDev& bd, int64_t rows, int k);
+
+cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q, const uint16_t* kv,
+                              const int32_t* idx, bool idx_local, int k, float sm_scale,
+                              uint16_t* out, float* lse, void* scratch, size_t scratch_bytes,
+                              int32_t* status, cudaStream_t stream);
+
+}  // namespace dsa
