@@ -1,0 +1,561 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA hot path (lightning indexer -> causal top-k ->
+sparse MLA attention) through libdsa.so on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl dsa|reference]
+
+One step is one pass of the whole path over one batch of synthetic input:
+  decode_B64_ctx32768 (default): one decode step of 64 sequences at context
+      32768 (one new query each), top-2048 -> metric "decode steps/s";
+  long_decode_B8_ctx202752: one decode step of 8 sequences near 202752;
+  prefill_T16384, tiny_prefill_T512_k128: a whole prefill -> tokens/s;
+  chunked_prefill_T65536_c8192: 8 chunks of 8192 queries -> tokens/s.
+Inputs are drawn on the device (seeded) and stay resident in HBM; the
+decode working set (2.96 GB of caches) is far larger than L2, so no flush
+is needed between steps.  Rank 0 prints ONE JSON line.
+
+--impl reference times the fp64 CPU oracle (the method written out plainly,
+tests/ pins it) on the host cores on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode_B64_ctx32768"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# algorithmic work per unit (see the measurement section of the design doc)
+IDX_FLOP_PER_PAIR = 2 * 32 * 128            # 8192
+IDX_BYTES_PER_KEY = 128 * 2                 # one bf16 index key
+IDX_BYTES_PER_QUERY = 32 * 128 * 2 + 32 * 4  # q_idx + w
+ATT_FLOP_PER_SEL = 2 * 64 * 576 + 2 * 64 * 512   # 139264
+ATT_BYTES_PER_SEL = 576 * 2                 # one gathered latent row
+ATT_BYTES_PER_QUERY = 64 * 576 * 2 + 64 * 512 * 2  # q in + out
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    p.add_argument("--impl", default="dsa", choices=["dsa", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kernel-reps", type=int, default=20)
+    return p.parse_args()
+
+
+def default_steps(wl: W.Workload):
+    return (300, 10) if wl.kind == "decode" else (20, 3)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- workloads --
+
+def metric_for(wl: W.Workload):
+    if wl.kind == "decode":
+        return f"decode steps/s ({wl.B} seqs x {wl.ctx} ctx, top-{wl.k}; % of HBM roofline)", "steps/s"
+    if wl.kind == "prefill":
+        return f"prefill tokens/s (T={wl.ctx}, top-{wl.k}; % of bf16 tensor roofline)", "tokens/s"
+    return f"chunked prefill tokens/s (T={wl.ctx} in {wl.ctx // wl.n_new} chunks, top-{wl.k})", "tokens/s"
+
+
+def base_config(wl: W.Workload, world: int):
+    return {"workload": wl.name, "batch": wl.B, "ctx": wl.ctx, "queries_per_seq": wl.n_new, "topk": wl.k,
+            "l2": "no flush: inputs larger than L2" if wl.kind == "decode" else
+            "no flush: the one sequence's keys and latent cache are L2-resident by design",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+class Case:
+    """The device inputs of one workload and its step function."""
+
+    def __init__(self, wl: W.Workload, seed: int, device):
+        import torch
+
+        import sparse_attention_gb300 as dsa
+        self.wl, self.dev = wl, device
+        self.calls = []          # (batch, slices) per dsa_forward call of one step
+        if wl.kind == "decode":
+            self.bt = W.make_batch_torch([wl.ctx] * wl.B, [1] * wl.B, wl.k, seed, key_kind=wl.key_kind,
+                                         device=device, name=wl.name)
+            bt = self.bt
+            # decode steps cycle over the last `steps` positions of the cache
+            self.ctx_variants = [torch.full((wl.B,), wl.ctx - wl.steps + 1 + j, dtype=torch.int32, device=device)
+                                 for j in range(wl.steps)]
+            self.batches = [dsa.Batch(bt.q_off, c, 1, wl.ctx, bt.stride, total_q=wl.B) for c in self.ctx_variants]
+            self.positions = [[wl.ctx - wl.steps + j] * wl.B for j in range(wl.steps)]
+            self.units_per_step = 1            # one decode step of the whole batch
+        elif wl.kind == "prefill":
+            self.bt = W.make_batch_torch([wl.ctx], [wl.n_new], wl.k, seed, key_kind=wl.key_kind, device=device,
+                                         name=wl.name)
+            bt = self.bt
+            self.batches = [dsa.Batch(bt.q_off, bt.ctx_len, wl.n_new, wl.ctx, bt.stride, total_q=wl.n_new)]
+            self.positions = [list(range(wl.ctx - wl.n_new, wl.ctx))]
+            self.units_per_step = wl.n_new
+        else:  # chunked prefill
+            T, C = wl.ctx, wl.n_new
+            self.bt = W.make_batch_torch([T], [T], wl.k, seed, key_kind=wl.key_kind, device=device, name=wl.name)
+            bt = self.bt
+            self.batches, self.positions = [], []
+            for c in range(T // C):
+                qo = torch.tensor([0, C], dtype=torch.int32, device=device)
+                cl = torch.tensor([C * (c + 1)], dtype=torch.int32, device=device)
+                self.batches.append(dsa.Batch(qo, cl, C, C * (c + 1), bt.stride, total_q=C))
+                self.positions.append(list(range(C * c, C * (c + 1))))
+            self.units_per_step = T
+        self.metric, self.unit = metric_for(wl)
+        self.max_rows = max(b.total_q for b in self.batches)
+        self.out = torch.empty((self.max_rows, 64, 512), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((self.max_rows, 64), dtype=torch.float32, device=device)
+        self.ws = [dsa.workspace(b, wl.k, device=device) for b in self.batches]
+        self.dsa = dsa
+
+    def _slices(self, j):
+        """query-side tensors of call j (chunked prefill slices the queries)."""
+        bt, wl = self.bt, self.wl
+        if self.wl.kind == "chunked_prefill":
+            C = wl.n_new
+            s = slice(C * j, C * (j + 1))
+            return bt.q_idx[s], bt.w[s], bt.q[s]
+        return bt.q_idx, bt.w, bt.q
+
+    def step(self, i=0):
+        """One step of the workload: every dsa_forward call it needs."""
+        wl = self.wl
+        if wl.kind == "decode":
+            j = i % len(self.batches)
+            calls = [j]
+        else:
+            calls = range(len(self.batches))
+        for j in calls:
+            q_idx, w, q = self._slices(j)
+            b = self.batches[j]
+            self.dsa.forward(b, q_idx, w, self.bt.k_idx, q, self.bt.kv, wl.k, self.bt.sm_scale,
+                             self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j])
+
+    # algorithmic work of one step
+    def work(self):
+        wl = self.wl
+        calls = [0] if wl.kind == "decode" else range(len(self.batches))
+        idx_flop = idx_bytes = att_flop = att_bytes = topk_bytes = 0
+        for j in calls:
+            pos = self.positions[j]
+            pairs = sum(t + 1 for t in pos)
+            sel = sum(min(wl.k, t + 1) for t in pos)
+            idx_flop += IDX_FLOP_PER_PAIR * pairs
+            att_flop += ATT_FLOP_PER_SEL * sel
+            att_bytes += ATT_BYTES_PER_SEL * sel + ATT_BYTES_PER_QUERY * len(pos)
+            topk_bytes += 4 * pairs + 4 * wl.k * len(pos)
+            if wl.kind == "decode":
+                idx_bytes += IDX_BYTES_PER_KEY * sum(t + 1 for t in pos) + IDX_BYTES_PER_QUERY * len(pos)
+            else:   # one sequence: keys read once per call (they stay in L2 across query groups)
+                idx_bytes += IDX_BYTES_PER_KEY * (max(pos) + 1) + IDX_BYTES_PER_QUERY * len(pos)
+        return dict(idx_flop=idx_flop, idx_bytes=idx_bytes, att_flop=att_flop, att_bytes=att_bytes,
+                    topk_bytes=topk_bytes)
+
+    def kernel_times_us(self, reps: int):
+        """Average device time of each step call (indexer, top-k, attention)
+        with CUDA events on the launching stream."""
+        import torch
+        dsa, wl = self.dsa, self.wl
+        stream = torch.cuda.current_stream()
+        j = 0
+        b = self.batches[j]
+        q_idx, w, q = self._slices(j)
+        ld = (b.max_ctx + 3) // 4 * 4
+        scores = torch.empty((b.total_q, ld), dtype=torch.float32, device=self.dev)
+        idx = torch.empty((b.total_q, wl.k), dtype=torch.int32, device=self.dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        tot = [0.0, 0.0, 0.0]
+        for r in range(reps + 2):
+            ev[0].record(stream)
+            dsa.indexer_scores(b, q_idx, w, self.bt.k_idx, scores, ld=ld, ws=self.ws[j])
+            ev[1].record(stream)
+            dsa.topk(b, scores, wl.k, idx, ld=ld, ws=self.ws[j])
+            ev[2].record(stream)
+            dsa.sparse_mla_fwd(b, q, self.bt.kv, idx, wl.k, self.bt.sm_scale, self.out[:b.total_q],
+                               self.lse[:b.total_q], ws=self.ws[j])
+            ev[3].record(stream)
+            torch.cuda.synchronize()
+            if r >= 2:
+                for x in range(3):
+                    tot[x] += ev[x].elapsed_time(ev[x + 1]) * 1e3
+        return {"indexer": tot[0] / reps, "topk": tot[1] / reps, "sparse_mla": tot[2] / reps}
+
+    def kernel_work_one_call(self):
+        """Algorithmic work of the calls timed by kernel_times_us (call 0)."""
+        wl = self.wl
+        pos = self.positions[0]
+        pairs = sum(t + 1 for t in pos)
+        sel = sum(min(wl.k, t + 1) for t in pos)
+        if wl.kind == "decode":
+            ib = IDX_BYTES_PER_KEY * pairs + IDX_BYTES_PER_QUERY * len(pos)
+        else:
+            ib = IDX_BYTES_PER_KEY * (max(pos) + 1) + IDX_BYTES_PER_QUERY * len(pos)
+        return {
+            "indexer": dict(flop=IDX_FLOP_PER_PAIR * pairs, bytes=ib),
+            "topk": dict(flop=0, bytes=4 * pairs + 4 * wl.k * len(pos)),
+            "sparse_mla": dict(flop=ATT_FLOP_PER_SEL * sel,
+                               bytes=ATT_BYTES_PER_SEL * sel + ATT_BYTES_PER_QUERY * len(pos)),
+        }
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) around the timed region; the summary
+    uses the samples whose timestamps fall inside it."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def timed(self, t0: float, t1: float):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        import datetime
+        samples = []
+        for line in out.strip().splitlines():
+            r = [x.strip() for x in line.split(",")]
+            if len(r) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(r[1]), float(r[2]), r[5:9]))
+            except ValueError:
+                continue
+        inside = [x for x in samples if self.window and self.window[0] - 0.05 <= x[0] <= self.window[1] + 0.05]
+        scope = "timed region"
+        if len(inside) < 2:      # a short timed region: use the busy period around it
+            inside, scope = samples, "warm-up, timed region and per-kernel timing"
+        sm = [x[1] for x in inside]
+        reasons = sorted({n for x in inside for n, v in zip(self.REASONS, x[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(x[2] for x in inside) if inside else None,
+                "reasons": reasons, "samples": len(sm), "scope": scope}
+
+
+# ------------------------------------------------------------- cpu oracle --
+
+def host_sample(case: Case, n_seq: int):
+    """Copy a sample of the workload to the host as a numpy Batch (decode: the
+    first n_seq sequences; prefill: evenly spaced query rows)."""
+    import torch
+    bt, wl = case.bt, case.wl
+
+    def bits(t):
+        return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    if wl.kind == "decode":
+        ctx = wl.ctx
+        rows = slice(0, n_seq)
+        cache = slice(0, n_seq * bt.stride)
+        b = W.Batch(B=n_seq, stride=bt.stride, q_off=np.arange(n_seq + 1, dtype=np.int32),
+                    ctx_len=np.full(n_seq, ctx, np.int32), q_idx=bits(bt.q_idx[rows]),
+                    w=bt.w[rows].cpu().numpy(), k_idx=bits(bt.k_idx[cache]), q=bits(bt.q[rows]),
+                    kv=bits(bt.kv[cache]), k=wl.k, sm_scale=bt.sm_scale)
+        return b, list(range(n_seq)), n_seq / wl.B, f"{n_seq} of {wl.B} sequences of one decode step"
+    T = wl.ctx
+    b = W.Batch(B=1, stride=bt.stride, q_off=np.array([0, T], np.int32), ctx_len=np.array([T], np.int32),
+                q_idx=bits(bt.q_idx), w=bt.w.cpu().numpy(), k_idx=bits(bt.k_idx), q=bits(bt.q), kv=bits(bt.kv),
+                k=wl.k, sm_scale=bt.sm_scale)
+    rows = sorted(set(int(x) for x in np.linspace(0, T - 1, n_seq)))
+    return b, rows, len(rows), f"{len(rows)} evenly spaced query rows of the {T}-token prefill"
+
+
+def oracle_path_seconds(b, rows):
+    import oracle
+    t0 = time.perf_counter()
+    sc = oracle.indexer_scores(b, rows)
+    ix = oracle.topk(b, np.nan_to_num(sc.astype(np.float32), nan=0.0), rows=rows, k=b.k)
+    oracle.sparse_mla(b, ix, rows=rows)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case: Case, unit: str):
+    import oracle
+    n = 24 if case.wl.kind == "decode" else 48
+    b, rows, units, sample = host_sample(case, n)
+    secs = oracle_path_seconds(b, rows)
+    # units: decode -> fraction of one step; prefill -> query rows (tokens)
+    return {"value": units / secs, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": sample + f" (full path: indexer, top-k, attention; {secs:.1f} s in fp64)"}
+
+
+# --------------------------------------------------------------- reference --
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    wl = W.WORKLOADS[args.workload]
+    K, Wu = default_steps(wl)
+    K = args.steps if args.steps is not None else K
+    Wu = args.warmup if args.warmup is not None else Wu
+    # one bounded sample per step, drawn with the numpy recipe
+    if wl.kind == "decode":
+        ns = 1
+        b = W.make_batch_np([wl.ctx] * ns, [1] * ns, wl.k, wl.seed, key_kind=wl.key_kind)
+        rows = list(range(ns))
+        frac = ns / wl.B
+        sample = f"{ns} of {wl.B} sequences of one decode step per timed step"
+    else:
+        T = wl.ctx
+        nq = 4
+        b = W.make_batch_np([T], [T], wl.k, wl.seed, key_kind=wl.key_kind) if T <= 16384 else None
+        if b is None:
+            print(json.dumps({"impl": "reference", "unavailable": "oracle sample of this workload exceeds host memory"}))
+            return
+        rows = [int(x) for x in np.linspace(0, T - 1, nq)]
+        frac = nq
+        sample = f"{nq} evenly spaced query rows per timed step"
+    for _ in range(Wu):
+        oracle_path_seconds(b, rows)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_path_seconds(b, rows)
+    secs = (time.perf_counter() - t0) / K
+    value = frac / secs
+    metric, unit = metric_for(wl)
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": K, "warmup": Wu, "ms_per_step": 1e3 / value if unit == "steps/s" else 1e3 * secs,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": base_config(wl, 1),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- dsa --
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """dram bytes per launch recorded by an ncu capture, if the kernel's
+    source is unchanged since (profiles/ncu_traffic.txt)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"indexer": "indexer.cu", "topk": "topk.cu", "sparse_mla": "sparse_mla.cu"}[kernel]
+    with open(os.path.join(ROOT, "sparse_attention_gb300", "csrc", src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    for line in open(path):
+        kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
+        if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("src_sha") == sha:
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+def run_dsa(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from sparse_attention_gb300 import build as B
+    if rank == 0 or world == 1:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    import sparse_attention_gb300 as dsa
+    dsa.load_library()
+
+    wl = W.WORKLOADS[args.workload]
+    K, Wu = default_steps(wl)
+    K = args.steps if args.steps is not None else K
+    Wu = max(3, args.warmup if args.warmup is not None else Wu)
+    case = Case(wl, wl.seed + 1000 * rank, dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(Wu):
+        case.step(i)
+    barrier()
+    n0 = dsa.kernel_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_start = time.time()
+    e0.record(stream)
+    for i in range(K):
+        case.step(i)
+    e1.record(stream)
+    barrier()
+    clocks.timed(t_start, time.time())
+    launches = dsa.kernel_launch_count() - n0
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    status = dsa.read_device_status(case.ws[0])
+    units = case.units_per_step * K * world
+    value = units / (ms / 1e3)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(case, K, Wu, barrier, max_over_ranks, world)
+
+    # per-kernel device times and the roofline of the dominant kernel
+    times = case.kernel_times_us(args.kernel_reps)
+    clk = clocks.stop()
+    work = case.kernel_work_one_call()
+    peaks, peak_src = load_peaks()
+    dom = max(times, key=times.get)
+    kw = work[dom]
+    if wl.kind != "decode" and dom in ("indexer", "sparse_mla"):
+        achieved = kw["flop"] / (times[dom] * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"]}
+    else:
+        achieved = kw["bytes"] / (times[dom] * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    roof.update({"kernel": dom, "peak_source": f"{peak_src} ({'burst' if roof['bound'] == 'tensor' else 'copy'})",
+                 "traffic": traffic_from_profiles(dom, wl.name),
+                 "kernel_us": {k: round(v, 2) for k, v in times.items()},
+                 "algorithmic_per_launch": kw})
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(case, case.unit)
+    wk = case.work()
+    cfg = base_config(wl, world)
+    details = {"algorithmic_per_step": {"indexer_tflop": wk["idx_flop"] / 1e12,
+                                        "attention_tflop": wk["att_flop"] / 1e12,
+                                        "indexer_gb": wk["idx_bytes"] / 1e9, "attention_gb": wk["att_bytes"] / 1e9},
+               "device_status": status}
+    if wl.kind == "decode":
+        details["tokens_per_s"] = value * wl.B
+    line = {"metric": case.metric, "value": value, "unit": case.unit, "n_gpus": world, "steps": K, "warmup": Wu,
+            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": cfg, "roofline": roof, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": launches, "clocks": clk, "details": details}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
+    """Same metric through dsa.forward with the step's inputs copied in from
+    pinned host memory and the result read back, every step."""
+    import torch
+    wl, bt = case.wl, case.bt
+    stream = torch.cuda.current_stream()
+    if wl.kind == "decode":
+        host = {"q_idx": bt.q_idx.cpu().pin_memory(), "w": bt.w.cpu().pin_memory(), "q": bt.q.cpu().pin_memory()}
+        kv3 = bt.kv.view(wl.B, bt.stride, 576)
+        ki3 = bt.k_idx.view(wl.B, bt.stride, 128)
+        new_kv = kv3[:, wl.ctx - 1].cpu().pin_memory()
+        new_ki = ki3[:, wl.ctx - 1].cpu().pin_memory()
+        out_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + [new_kv, new_ki])
+        d2h = out_h.numel() * out_h.element_size()
+
+        def step(i):
+            bt.q_idx.copy_(host["q_idx"], non_blocking=True)
+            bt.w.copy_(host["w"], non_blocking=True)
+            bt.q.copy_(host["q"], non_blocking=True)
+            kv3[:, wl.ctx - 1].copy_(new_kv, non_blocking=True)
+            ki3[:, wl.ctx - 1].copy_(new_ki, non_blocking=True)
+            case.step(len(case.batches) - 1)
+            out_h.copy_(case.out, non_blocking=True)
+    else:
+        host = {"q_idx": bt.q_idx.cpu().pin_memory(), "w": bt.w.cpu().pin_memory(), "q": bt.q.cpu().pin_memory(),
+                "kv": bt.kv.cpu().pin_memory(), "k_idx": bt.k_idx.cpu().pin_memory()}
+        out_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def step(i):
+            for name, t in host.items():
+                getattr(bt, name).copy_(t, non_blocking=True)
+            case.step(i)
+            out_h.copy_(case.out, non_blocking=True)
+    for i in range(Wu):
+        step(i)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        step(i)
+    e1.record(stream)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    value = case.units_per_step * K * world / (ms / 1e3)
+    return {"value": value, "unit": case.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "sparse_attention_gb300.forward"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_dsa(args)
+
+
+if __name__ == "__main__":
+    main()

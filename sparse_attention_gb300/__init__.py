@@ -30,7 +30,7 @@ STATUS = {
     4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_BAD_BATCH", 7: "DSA_ERR_BAD_INDEX",
 }
 
-EXPORTS = ("dsa_status_string", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
+EXPORTS = ("dsa_status_string", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
            "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward")
 
 
@@ -62,6 +62,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     BP = ctypes.POINTER(DsaBatch)
     lib.dsa_status_string.restype = ctypes.c_char_p
     lib.dsa_status_string.argtypes = [i32]
+    lib.dsa_kernel_launch_count.restype = ctypes.c_uint64
+    lib.dsa_kernel_launch_count.argtypes = []
     lib.dsa_workspace_size.argtypes = [BP, i32, ctypes.POINTER(sz)]
     lib.dsa_reset_device_status.argtypes = [P, P]
     lib.dsa_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
@@ -70,7 +72,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_sparse_mla_fwd.argtypes = [BP, P, P, P, i32, f32, P, P, P, sz, P]
     lib.dsa_forward.argtypes = [BP, P, P, P, P, P, i32, f32, P, P, P, P, i64, P, sz, P]
     for name in EXPORTS:
-        if name != "dsa_status_string":
+        if name not in ("dsa_status_string", "dsa_kernel_launch_count"):
             getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -139,6 +141,11 @@ def _stream(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
     return stream.cuda_stream
+
+
+def kernel_launch_count() -> int:
+    """Kernels launched by libdsa.so in this process so far."""
+    return int(load_library().dsa_kernel_launch_count())
 
 
 def workspace_size(batch: Batch, k: int) -> int:

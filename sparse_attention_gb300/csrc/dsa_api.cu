@@ -2,12 +2,17 @@
 // documented in include/dsa.h): host-side argument checks, workspace
 // layout, and the launch sequence of dsa_forward.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 
 #include "internal.h"
 
 namespace dsa {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
 namespace {
 
 // Scores of one dsa_forward chunk are sized to stay resident in the 126 MB
@@ -92,6 +97,8 @@ const char* dsa_status_string(int s) {
         default: return "unknown dsa_status";
     }
 }
+
+uint64_t dsa_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 dsa_status dsa_workspace_size(const dsa_batch* batch, int k, size_t* bytes) {
     if (!bytes) return DSA_ERR_INVALID_ARG;

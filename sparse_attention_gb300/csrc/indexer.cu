@@ -292,7 +292,9 @@ cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, co
     dim3 grid(splits, groups, bd.B);
     indexer_kernel<NQ><<<grid, C::kThreads, C::kSmemBytes, stream>>>(bd, rr, tm_k, tm_q, w, scores, ld,
                                                                       scores_local ? 1 : 0, tps, status);
-    return cudaGetLastError();
+    const cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) count_launches(1);
+    return err;
 }
 
 }  // namespace

@@ -65,6 +65,9 @@ __device__ __forceinline__ int64_t buf_row(bool local, const SeqInfo& s, int b, 
     return local ? (int64_t)b * (rr.i1 - rr.i0) + (i - rr.i0) : (int64_t)s.q0 + i;
 }
 
+// Adds n to the process-wide count of kernels launched by this library.
+void count_launches(int n);
+
 // ------------------------------------------------------------ launchers --
 
 cudaError_t launch_indexer(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, const float* w,

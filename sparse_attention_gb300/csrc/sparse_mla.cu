@@ -277,10 +277,14 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
                                                              rows_per_seq, splits, per_split, sm_scale, out,
                                                              lse, part_o, part_lse, status);
     e = cudaGetLastError();
-    if (e != cudaSuccess || splits == 1) return e;
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    if (splits == 1) return e;
     merge_kernel<<<dim3(rows_per_seq, bd.B), 256, 0, stream>>>(bd, rr, rows_per_seq, splits, part_o, part_lse,
                                                               out, lse, status);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
 }
 
 }  // namespace dsa

@@ -204,7 +204,9 @@ cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, in
     dim3 grid(rows_per_seq, bd.B);
     topk_kernel<<<grid, kThreads, smem, stream>>>(bd, rr, scores, ld, scores_local ? 1 : 0, k, idx,
                                                   idx_local ? 1 : 0, smem_keys, status);
-    return cudaGetLastError();
+    const cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) count_launches(1);
+    return err;
 }
 
 }  // namespace dsa
