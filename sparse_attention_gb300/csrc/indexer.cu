@@ -234,36 +234,6 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-// 2-D bf16 tensor [rows, 128] with 256-byte rows, 128B swizzle, box {64, box_rows}.
-bool make_tmap_bf16_128(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {128, rows};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int NQ>
 cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, const float* w,
                       const uint16_t* k_idx, float* scores, int64_t ld, bool scores_local, int32_t* status,
@@ -284,8 +254,10 @@ cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, co
     }
     const int32_t splits = (tiles + tps - 1) / tps;
     CUtensorMap tm_k, tm_q;
-    if (!make_tmap_bf16_128(&tm_k, k_idx, (uint64_t)bd.B * (uint64_t)bd.stride, C::kBM)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16_128(&tm_q, q_idx, (uint64_t)bd.total_q * kHIdx, C::kN)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_2d(&tm_k, k_idx, kDIdx, (uint64_t)bd.B * (uint64_t)bd.stride, 64, C::kBM))
+        return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_2d(&tm_q, q_idx, kDIdx, (uint64_t)bd.total_q * kHIdx, 64, C::kN))
+        return cudaErrorInvalidValue;
     cudaError_t e =
         cudaFuncSetAttribute(indexer_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;

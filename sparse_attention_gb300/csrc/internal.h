@@ -1,5 +1,6 @@
 // internal.h -- definitions shared by the CUDA translation units of libdsa.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -64,6 +65,12 @@ __device__ __forceinline__ bool load_seq(const BatchDev& bd, int b, int32_t* sta
 __device__ __forceinline__ int64_t buf_row(bool local, const SeqInfo& s, int b, int32_t i, RowRange rr) {
     return local ? (int64_t)b * (rr.i1 - rr.i0) + (i - rr.i0) : (int64_t)s.q0 + i;
 }
+
+// Tensor map of a row-major 2-D bf16 tensor [rows, inner] (row stride inner*2
+// bytes), 128-byte swizzle, box {box_inner, box_rows}.  False if the driver
+// entry point is unavailable or rejects the arguments.
+bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                       uint32_t box_rows);
 
 // Adds n to the process-wide count of kernels launched by this library.
 void count_launches(int n);

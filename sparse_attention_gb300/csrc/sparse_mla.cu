@@ -1,5 +1,5 @@
 // sparse_mla.cu -- sparse MLA attention over the selected latent rows,
-// absorbed form.
+// absorbed form, on the 5th-generation tensor cores.
 //
 // For query row t and head h, over the selected positions s_j = idx[t, j]:
 //   l_j   = sm_scale * q[t,h,:] . kv[s_j, :]          (576 = 512 latent + 64 rope)
@@ -9,50 +9,84 @@
 // is one stream shared by all heads; section 2.5: 576-wide cached rows; the
 // GLM-5 explainer page: the top-2048 ids only drive the gather.)
 //
-// This file holds the CUDA-core path: one CTA per (query row, split of the
-// selected list) with the 64-head query block resident in shared memory;
-// selected rows are gathered 32 at a time with 16-byte loads, logits and
-// the running softmax are fp32, and the output accumulates in registers.
-// When a query's selected list is split over several CTAs, each writes an
-// fp32 partial (normalised output and lse) to scratch and a merge kernel
-// combines them with log-sum-exp weights.
+// One CTA per (query row, segment of its selected list).  With only 64
+// heads, a heads-as-M MMA would run at M = 64, half the tensor rate; so the
+// products are taken transposed, with the 128 gathered rows of a block on
+// the M = 128 side:
+//   S^T[128 rows, 64 heads] = KV_blk[128, 576] . Q^T           (K-major A and B)
+//   O^T[512, 64]           += V_blk^T[512, 128] . P^T[128, 64]  (MN-major A and B)
+// V_blk is the first 512 columns of the same gathered tile, so every row is
+// read from memory once.  Roles by warp:
+//   warp 0      producer: validates the block's indices and gathers the
+//               576-wide rows with 16-byte cp.async copies (8 lanes per
+//               128-byte row piece, coalesced) into nine 64-column chunks
+//               laid out 128B-swizzled; Q once by TMA
+//   warp 1      TMEM owner and MMA issuer
+//   warps 2..5  softmax: thread = one gathered row; the per-head block max
+//               is a warp max (redux.sync) plus a cross-warp max through
+//               shared memory; p = exp2(s*c - m) in fp32, written as bf16
+//               P^T over the RoPE chunk (no longer needed once S^T is
+//               done); O^T is rescaled in TMEM only when a head's running
+//               max grows by more than 2^8; final normalisation and store.
+// A single 144 KiB row tile fits next to Q (72 KiB); it is refilled chunk
+// by chunk as soon as the MMAs that read each chunk have completed.
+// Split-K partials (for few query rows) are merged by merge_kernel.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 #include <cmath>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRows = 32;                       // selected rows per block
-constexpr int kQStride = kDQK + 8;              // padded bf16 row stride (bank spread)
-constexpr int kKVStride = kDQK + 8;
-constexpr int kPStride = kRows + 1;
+constexpr int kBlk = 128;                    // gathered rows per block (MMA M)
+constexpr int kChunks = kDQK / 64;           // 9 column chunks of 64
+constexpr int kVChunks = kDV / 64;           // the first 8 hold V
+constexpr int kKVChunkBytes = kBlk * 128;    // 16 KiB
+constexpr int kQChunkBytes = kH * 128;       // 8 KiB
+constexpr int kThreads = 192;
+constexpr float kRescaleLog2 = 8.0f;         // rescale O only when a max grows by > 2^8
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
-struct AttnSmem {
-    __nv_bfloat16 q[kH * kQStride];
-    __nv_bfloat16 kv[kRows * kKVStride];
-    float p[kH * kPStride];
-    float m[kH], l[kH], alpha[kH];
-    int32_t sel[kRows];
-};
-
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
-    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-}
+// shared memory layout (offsets from a 1024-aligned base)
+constexpr int kOffKV = 0;
+constexpr int kOffQ = kOffKV + kChunks * kKVChunkBytes;       // 147456
+constexpr int kOffIdx = kOffQ + kChunks * kQChunkBytes;       // int32 [2][128]
+constexpr int kOffWmax = kOffIdx + 2 * kBlk * 4;              // float [4][64]
+constexpr int kOffM = kOffWmax + 4 * kH * 4;                  // float m_use[64]
+constexpr int kOffAlpha = kOffM + kH * 4;                     // float alpha[64]
+constexpr int kOffL = kOffAlpha + kH * 4;                     // float [4][64], then l_tot[64]
+constexpr int kOffMisc = kOffL + 5 * kH * 4;                  // u32: tmem base, abort, nblk
+constexpr int kOffBar = kOffMisc + 16;
+constexpr int kBarQ = 0;
+constexpr int kBarKV = 1;                                     // [9]: chunk c landed
+constexpr int kBarPair = kBarKV + kChunks;                    // [4]: chunks 2i, 2i+1 consumed
+constexpr int kBarS = kBarPair + 4;                           // S^T ready
+constexpr int kBarP = kBarS + 1;                              // P^T written (128 arrivals)
+constexpr int kBarO = kBarP + 1;                              // PV of a block done (chunk 8 free)
+constexpr int kBarIdx = kBarO + 1;                            // [2]: indices of a block published
+constexpr int kBarDrain = kBarIdx + 2;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;                                // O^T: 4 blocks x 64 columns
+constexpr uint32_t kTmemS = 256;                              // S^T: 64 columns
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_simt_kernel(const BatchDev bd, const RowRange rr, const uint16_t* __restrict__ q,
-                           const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx, const int idx_local,
-                           const int k, const int rows_per_seq, const int splits, const int per_split,
-                           const float sm_scale,
-                           uint16_t* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
-                           float* __restrict__ part_lse, int32_t* status) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    AttnSmem& S = *reinterpret_cast<AttnSmem*>(smem_raw);
+    sparse_mla_tc_kernel(const BatchDev bd, const RowRange rr, const __grid_constant__ CUtensorMap tm_q,
+                         const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
+                         const int idx_local, const int k, const int rows_per_seq, const int splits,
+                         const int per_split, const float sm_scale, uint16_t* __restrict__ out,
+                         float* __restrict__ lse, float* __restrict__ part_o, float* __restrict__ part_lse,
+                         int32_t* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
     const int b = blockIdx.y;
     SeqInfo sq;
     if (!load_seq(bd, b, status, sq)) return;
@@ -60,136 +94,359 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sp = (int)(blockIdx.x % splits);
     if (i >= min(rr.i1, sq.nq)) return;
     const int32_t t = sq.ctx - sq.nq + i;
-    const int64_t grow = (int64_t)sq.q0 + i;                       // packed query row
-    const int32_t* sel_row = idx + buf_row(idx_local, sq, b, i, rr) * (int64_t)k;
-    const int j_begin = sp * per_split, j_end = min(k, j_begin + per_split);
-    const uint16_t* kv_seq = kv + (int64_t)b * bd.stride * kDQK;
-    const int tid = threadIdx.x;
+    const int64_t grow = (int64_t)sq.q0 + i;
+    const int32_t* sel = idx + buf_row(idx_local, sq, b, i, rr) * (int64_t)k;
+    const int j_begin = sp * per_split;
+    const int j_end = min(k, j_begin + per_split);
+    const int32_t row0 = (int32_t)((int64_t)b * bd.stride);       // cache row of position 0
+    const int64_t prow = ((int64_t)b * rows_per_seq + (i - rr.i0)) * splits + sp;   // split partial row
 
-    // query block -> shared memory
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(q + grow * kH * kDQK);
-        for (int e = tid; e < kH * kDQK / 8; e += kThreads) {
-            const int h = e / (kDQK / 8), c = e % (kDQK / 8);
-            *reinterpret_cast<uint4*>(&S.q[h * kQStride + c * 8]) = __ldg(src + e);
-        }
-    }
-    if (tid < kH) {
-        S.m[tid] = -INFINITY;
-        S.l[tid] = 0.f;
-    }
-    // thread roles
-    const int qk_h = tid >> 2, qk_r = tid & 3;    // QK: head, row phase
-    const int pv_h = tid >> 2, pv_c = tid & 3;    // PV: head, column phase
-    float acc[128];
-#pragma unroll
-    for (int c = 0; c < 128; ++c) acc[c] = 0.f;
+    const uint32_t sKV = smem_u32(smem + kOffKV);
+    const uint32_t sQ = smem_u32(smem + kOffQ);
+    int32_t* s_idx = reinterpret_cast<int32_t*>(smem + kOffIdx);
+    float* s_wmax = reinterpret_cast<float*>(smem + kOffWmax);
+    float* s_m = reinterpret_cast<float*>(smem + kOffM);
+    float* s_alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+    float* s_l = reinterpret_cast<float*>(smem + kOffL);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
+    const uint32_t bar0 = smem_u32(smem + kOffBar);
+    auto bar = [&](int n) { return bar0 + 8u * (uint32_t)n; };
+    const uint32_t warp = warp_id(), lane = lane_id();
 
-    for (int jb = j_begin; jb < j_end; jb += kRows) {
-        __syncthreads();
-        if (tid < kRows) {
-            const int j = jb + tid;
-            int32_t s = (j < j_end) ? __ldg(sel_row + j) : -1;
-            if (s < -1 || s > t) {
-                latch_status(status, DSA_ERR_BAD_INDEX);
-                s = -1;
-            }
-            S.sel[tid] = s;
-        }
-        __syncthreads();
-        // gather the selected rows (16 B per load)
-        for (int e = tid; e < kRows * (kDQK / 8); e += kThreads) {
-            const int r = e / (kDQK / 8), c = e % (kDQK / 8);
-            const int32_t s = S.sel[r];
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (s >= 0) v = __ldg(reinterpret_cast<const uint4*>(kv_seq + (int64_t)s * kDQK) + c);
-            *reinterpret_cast<uint4*>(&S.kv[r * kKVStride + c * 8]) = v;
-        }
-        __syncthreads();
-        // logits: head qk_h against rows qk_r + 4u
-        {
-            float dot[8];
+    // blocks of this segment: up to its last valid entry
+    if (warp == 0) {
+        int last = -1;
+        for (int j = j_begin + (int)lane; j < j_end; j += 32)
+            if (__ldg(sel + j) >= 0) last = j;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) dot[u] = 0.f;
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(&S.q[qk_h * kQStride]);
-            for (int d2 = 0; d2 < kDQK / 2; ++d2) {
-                const float2 qv = bf2_to_f2(qrow[d2]);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float2 kvv =
-                        bf2_to_f2(reinterpret_cast<const uint32_t*>(&S.kv[(qk_r + 4 * u) * kKVStride])[d2]);
-                    dot[u] = fmaf(qv.x, kvv.x, dot[u]);
-                    dot[u] = fmaf(qv.y, kvv.y, dot[u]);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int r = qk_r + 4 * u;
-                S.p[qk_h * kPStride + r] = (S.sel[r] >= 0) ? dot[u] * sm_scale : -INFINITY;
-            }
-        }
-        __syncthreads();
-        // online softmax, one thread per head
-        if (tid < kH) {
-            float mx = S.m[tid];
-            for (int r = 0; r < kRows; ++r) mx = fmaxf(mx, S.p[tid * kPStride + r]);
-            const float alpha = (mx == -INFINITY) ? 1.f : expf(S.m[tid] - mx);
-            float sum = 0.f;
-            for (int r = 0; r < kRows; ++r) {
-                const float lg = S.p[tid * kPStride + r];
-                const float pr = (lg == -INFINITY) ? 0.f : expf(lg - mx);
-                S.p[tid * kPStride + r] = pr;
-                sum += pr;
-            }
-            S.l[tid] = S.l[tid] * alpha + sum;
-            S.m[tid] = mx;
-            S.alpha[tid] = alpha;
-        }
-        __syncthreads();
-        // O[h, :] = alpha * O + P @ V  (columns 2*(pv_c + 4c), +1)
-        {
-            const float alpha = S.alpha[pv_h];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) acc[c] *= alpha;
-            for (int r = 0; r < kRows; ++r) {
-                const float pr = S.p[pv_h * kPStride + r];
-                const uint32_t* vrow = reinterpret_cast<const uint32_t*>(&S.kv[r * kKVStride]);
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const float2 v = bf2_to_f2(vrow[pv_c + 4 * c]);
-                    acc[2 * c] = fmaf(pr, v.x, acc[2 * c]);
-                    acc[2 * c + 1] = fmaf(pr, v.y, acc[2 * c + 1]);
-                }
-            }
-        }
+        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+        if (lane == 0) misc[2] = last < j_begin ? 0u : (uint32_t)((last - j_begin) / kBlk + 1);
     }
+    if (threadIdx.x == 0) {
+        for (int n = 0; n < kNumBars; ++n) mbar_init(bar(n), 1);
+        mbar_init(bar(kBarP), 128);
+        mbar_init(bar(kBarIdx), 32);
+        mbar_init(bar(kBarIdx + 1), 32);
+        for (int c = 0; c < kChunks; ++c) mbar_init(bar(kBarKV + c), 32);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x >= 64 && threadIdx.x < 64 + kH) s_m[threadIdx.x - 64] = -INFINITY;
+    tc_fence_before();
     __syncthreads();
-    const float l = S.l[pv_h], m = S.m[pv_h];
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const float row_lse = l > 0.f ? m + logf(l) : -INFINITY;
-    if (splits == 1) {
-        uint32_t* o = reinterpret_cast<uint32_t*>(out + (grow * kH + pv_h) * kDV);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * c] * inv, acc[2 * c + 1] * inv);
-            o[pv_c + 4 * c] = *reinterpret_cast<const uint32_t*>(&v);
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const int nblk = (int)misc[2];
+    const float c2 = sm_scale * kLog2e;      // logits in log2 units
+
+    if (warp == 0) {
+        // ----------------------------------------------------------- producer
+        const bool leader = lane == 0;
+        if (leader) {
+            prefetch_tmap(&tm_q);
+            if (nblk > 0) {
+                mbar_arrive_expect_tx(bar(kBarQ), kChunks * kQChunkBytes);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_2d(sQ + c * kQChunkBytes, &tm_q, bar(kBarQ), c * 64, (int32_t)(grow * kH));
+            }
         }
-        if (lse && pv_c == 0) lse[grow * kH + pv_h] = row_lse;
-    } else {
-        const int64_t prow = ((int64_t)b * rows_per_seq + (i - rr.i0)) * splits + sp;
-        float2* o = reinterpret_cast<float2*>(part_o + (prow * kH + pv_h) * kDV);
+        int issued = 0;
+        for (int jb = 0; jb < nblk; ++jb) {
+            const uint32_t ph = (uint32_t)jb & 1u;
+            // indices of this block: validated, -1 where invalid or past the segment
+            int32_t v[4];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) o[pv_c + 4 * c] = make_float2(acc[2 * c] * inv, acc[2 * c + 1] * inv);
-        if (pv_c == 0) part_lse[prow * kH + pv_h] = row_lse;
+            for (int u = 0; u < 4; ++u) {
+                const int j = j_begin + jb * kBlk + u * 32 + (int)lane;
+                int32_t s = (j < j_end) ? __ldg(sel + j) : -1;
+                if (s < -1 || s > t) {
+                    latch_status(status, DSA_ERR_BAD_INDEX);
+                    s = -1;
+                }
+                v[u] = s;
+            }
+            // buffer jb & 1 was last read by the softmax of block jb - 2,
+            // which finished before PV(jb - 1) started
+            bool ok = jb == 0 || (!misc[1] && mbar_wait(bar(kBarPair), ph ^ 1u));
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                latch_status(status, DSA_ERR_TIMEOUT);
+                misc[1] = 1;
+                break;
+            }
+            int32_t* ib = s_idx + (jb & 1) * kBlk;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ib[u * 32 + lane] = v[u];
+            __syncwarp();
+            mbar_arrive(bar(kBarIdx + (jb & 1)));
+            const uint8_t* kv_seq = reinterpret_cast<const uint8_t*>(kv) + (int64_t)row0 * (kDQK * 2);
+            for (int c = 0; c < kChunks && ok; ++c) {
+                // chunk c of the previous block must have been consumed
+                if (jb > 0) {
+                    const uint32_t fb = c < kVChunks ? bar(kBarPair + c / 2) : bar(kBarO);
+                    ok = !misc[1] && mbar_wait(fb, ph ^ 1u);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
+                // 4 rows x 8 pieces of 16 B per warp instruction
+                const uint32_t dst = sKV + c * kKVChunkBytes;
+                const int piece = (int)(lane & 7u);
+#pragma unroll 4
+                for (int r4 = 0; r4 < kBlk; r4 += 4) {
+                    const int rr_ = r4 + (int)(lane >> 3);
+                    const int32_t s = ib[rr_];
+                    const uint8_t* src = kv_seq + (int64_t)(s >= 0 ? s : 0) * (kDQK * 2) + c * 128 + piece * 16;
+                    cp_async_16(dst + rr_ * 128 + ((piece ^ (rr_ & 7)) << 4), src);
+                }
+                cp_async_arrive(bar(kBarKV + c));
+                ++issued;
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                latch_status(status, DSA_ERR_TIMEOUT);
+                misc[1] = 1;
+                break;
+            }
+        }
+        if (misc[1]) {
+            // wind down: let every copy this warp started land first
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            if (leader && nblk > 0) mbar_wait(bar(kBarQ), 0);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA
+        if (elect_one()) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kH, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kH, true, true);
+            bool ok = nblk == 0 || mbar_wait(bar(kBarQ), 0);
+            tc_fence_after();
+            for (int jb = 0; ok && jb < nblk; ++jb) {
+                const uint32_t ph = (uint32_t)jb & 1u;
+                // S^T = KV_blk . Q^T over the 9 chunks of 64 columns
+                for (int c = 0; c < kChunks; ++c) {
+                    if (misc[1] || !mbar_wait(bar(kBarKV + c), ph)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();      // cp.async data -> tensor-core reads
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc_sw128(sKV + c * kKVChunkBytes + kk * 32, 16, 1024);
+                        const uint64_t bdsc = sdesc_sw128(sQ + c * kQChunkBytes + kk * 32, 16, 1024);
+                        mma_bf16_ss(tmem + kTmemS, ad, bdsc, idesc_s, (c | kk) != 0);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar(kBarS));
+                // O^T += V^T . P^T once the softmax has written P^T
+                if (misc[1] || !mbar_wait(bar(kBarP), ph)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sP = sKV + kVChunks * kKVChunkBytes;
+                for (int dv = 0; dv < 4; ++dv) {
+#pragma unroll
+                    for (int kk = 0; kk < kBlk / 16; ++kk) {
+                        const uint64_t ad =
+                            sdesc_sw128(sKV + (2 * dv) * kKVChunkBytes + kk * 2048, kKVChunkBytes, 1024);
+                        const uint64_t bdsc = sdesc_sw128(sP + kk * 2048, 1024, 1024);
+                        mma_bf16_ss(tmem + kTmemO + dv * kH, ad, bdsc, idesc_o, (jb | kk) != 0);
+                    }
+                    mma_commit(bar(kBarPair + dv));
+                }
+                mma_commit(bar(kBarO));
+            }
+            if (!ok) {
+                latch_status(status, DSA_ERR_TIMEOUT);
+                misc[1] = 1;
+            }
+            // every MMA this thread issued has finished once drain completes
+            mma_commit(bar(kBarDrain));
+            mbar_wait(bar(kBarDrain), 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- softmax
+        const uint32_t lq = warp & 3u;                 // TMEM lane quarter
+        const int r = (int)(lq * 32 + lane);           // row of the block
+        const int st = (int)threadIdx.x - 64;          // 0..127 among the softmax threads
+        const uint32_t lane_base = (lq * 32u) << 16;
+        float lsum[kH];
+#pragma unroll
+        for (int h = 0; h < kH; ++h) lsum[h] = 0.f;
+        bool ok = true;
+        for (int jb = 0; jb < nblk; ++jb) {
+            const uint32_t ph = (uint32_t)jb & 1u;
+            const bool got = !misc[1] && mbar_wait(bar(kBarIdx + (jb & 1)), ((uint32_t)jb >> 1) & 1u) &&
+                             mbar_wait(bar(kBarS), ph);
+            // every abort is agreed by all 128 softmax threads before any
+            // named barrier, so none of them can be left waiting at one
+            if (named_bar_or(3, 128, !got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const bool valid = s_idx[(jb & 1) * kBlk + r] >= 0;
+            float s[kH];
+            {
+                uint32_t u[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + kTmemS, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 32; ++h) s[h] = valid ? __uint_as_float(u[h]) : -INFINITY;
+                tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + 32, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 32; ++h) s[32 + h] = valid ? __uint_as_float(u[h]) : -INFINITY;
+            }
+            // per-head block max: a warp max, then across the four warps
+#pragma unroll
+            for (int h = 0; h < kH; ++h) {
+                const float m = warp_max_f32(s[h]);
+                if (lane == 0) s_wmax[lq * kH + h] = m;
+            }
+            named_bar_sync(1, 128);
+            bool need = false;
+            if (st < kH) {
+                const float mb =
+                    fmaxf(fmaxf(s_wmax[st], s_wmax[kH + st]), fmaxf(s_wmax[2 * kH + st], s_wmax[3 * kH + st]));
+                const float mold = s_m[st];
+                const float mnew = mb * c2;
+                float alpha = 1.f;
+                if (mb > -INFINITY && (mold == -INFINITY || mnew > mold + kRescaleLog2)) {
+                    alpha = exp2f(mold - mnew);              // 0 when nothing was seen yet
+                    s_m[st] = mnew;
+                    need = true;
+                }
+                s_alpha[st] = alpha;
+            }
+            const bool rescale = named_bar_or(2, 128, need);
+            if (rescale) {
+                // O^T holds the blocks before jb once PV(jb - 1) has completed
+                const bool w = jb == 0 || mbar_wait(bar(kBarO), ph ^ 1u);
+                if (named_bar_or(3, 128, !w)) {
+                    ok = false;
+                    break;
+                }
+                if (jb > 0) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cb = 0; cb < 8; ++cb) {
+                        uint32_t u[32];
+                        const uint32_t ta = tmem + lane_base + kTmemO + cb * 32;
+                        tmem_ld_32x32b_x32(ta, u);
+                        tmem_ld_wait();
+                        const float* al = s_alpha + (cb & 1) * 32;
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * al[x]);
+                        tmem_st_32x32b_x32(ta, u);
+                    }
+                    tmem_st_wait();
+                }
+#pragma unroll
+                for (int h = 0; h < kH; ++h) lsum[h] *= s_alpha[h];
+            }
+            // P^T row r over the RoPE chunk, 128B-swizzled (MN-major B operand)
+            uint8_t* prow = smem + kOffKV + kVChunks * kKVChunkBytes + r * 128;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int h = c8 * 8 + e;
+                    p[e] = valid ? exp2f(fmaf(s[h], c2, -s_m[h])) : 0.f;
+                    lsum[h] += p[e];
+                }
+                uint4 pk;
+                pk.x = pack_bf16x2(p[0], p[1]);
+                pk.y = pack_bf16x2(p[2], p[3]);
+                pk.z = pack_bf16x2(p[4], p[5]);
+                pk.w = pack_bf16x2(p[6], p[7]);
+                *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = pk;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(kBarP));
+        }
+        if (!ok) {
+            latch_status(status, DSA_ERR_TIMEOUT);
+            misc[1] = 1;
+        }
+        // ------------------------------------------------------- epilogue
+        // l: the per-thread partial sums reduced over the 128 rows
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+            float v = lsum[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) s_l[lq * kH + h] = v;
+        }
+        bool w = ok && (nblk == 0 || mbar_wait(bar(kBarO), ((uint32_t)nblk - 1u) & 1u));
+        w = __all_sync(0xffffffffu, w);
+        named_bar_sync(1, 128);
+        if (st < kH) {
+            const float lt = s_l[st] + s_l[kH + st] + s_l[2 * kH + st] + s_l[3 * kH + st];
+            s_l[4 * kH + st] = lt;
+            const float ls = lt > 0.f ? (s_m[st] + log2f(lt)) * kLn2 : -INFINITY;
+            if (splits == 1) {
+                if (lse) lse[grow * kH + st] = ls;
+            } else {
+                part_lse[prow * kH + st] = ls;
+            }
+        }
+        named_bar_sync(1, 128);
+        if (w) {
+            tc_fence_after();
+            const float* lt = s_l + 4 * kH;
+            for (int dv = 0; dv < 4; ++dv) {
+                const int d = dv * 128 + r;                   // output column of this thread
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t u[32];
+                    if (nblk > 0) {
+                        tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + dv * kH + half * 32, u);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) u[x] = 0u;
+                    }
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        const int h = half * 32 + x;
+                        const float l = lt[h];
+                        const float o = l > 0.f ? __uint_as_float(u[x]) / l : 0.f;
+                        if (splits == 1) {
+                            const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+                            out[(grow * kH + h) * kDV + d] = *reinterpret_cast<const uint16_t*>(&ob);
+                        } else {
+                            part_o[(prow * kH + h) * kDV + d] = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 // out = sum_s exp(lse_s - L) * o_s, L = log sum_s exp(lse_s)
 __global__ void __launch_bounds__(256)
     merge_kernel(const BatchDev bd, const RowRange rr, const int rows_per_seq, const int splits,
-                 const float* __restrict__ part_o,
-                 const float* __restrict__ part_lse, uint16_t* __restrict__ out, float* __restrict__ lse,
-                 int32_t* status) {
+                 const float* __restrict__ part_o, const float* __restrict__ part_lse, uint16_t* __restrict__ out,
+                 float* __restrict__ lse, int32_t* status) {
     const int b = blockIdx.y;
     SeqInfo sq;
     if (!load_seq(bd, b, status, sq)) return;
@@ -232,12 +489,13 @@ __global__ void __launch_bounds__(256)
     if (lse && part == 0) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
-// number of CTAs per query row: enough to give ~2 CTAs per SM
+// CTAs per query row: about one CTA per SM in total (one CTA fills an SM's
+// shared memory), at least one 128-row block each.
 int choose_splits(int64_t rows, int k) {
     if (rows <= 0) return 1;
-    const int64_t want = (2 * kNumSMs + rows - 1) / rows;
-    const int max_by_k = std::max(1, k / 64);
-    return (int)std::min<int64_t>(std::max<int64_t>(1, want), std::min(32, max_by_k));
+    const int64_t want = (kNumSMs + rows - 1) / rows;
+    const int max_by_k = std::max(1, (k + kBlk - 1) / kBlk);
+    return (int)std::min<int64_t>(std::max<int64_t>(1, want), std::min(16, max_by_k));
 }
 
 }  // namespace
@@ -259,7 +517,7 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
     if (rows_per_seq <= 0) return cudaSuccess;
     const int64_t rows = (int64_t)rows_per_seq * bd.B;
     const int splits = choose_splits((int64_t)bd.B * bd.max_q, k);
-    const int per_split = ((k + splits - 1) / splits + kRows - 1) / kRows * kRows;
+    const int per_split = ((k + splits - 1) / splits + kBlk - 1) / kBlk * kBlk;
     float* part_o = nullptr;
     float* part_lse = nullptr;
     if (splits > 1) {
@@ -268,14 +526,15 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
         part_o = static_cast<float*>(scratch);
         part_lse = part_o + (size_t)rows * splits * kH * kDV;
     }
-    const size_t smem = sizeof(AttnSmem);
+    CUtensorMap tm_q;
+    if (!make_tmap_bf16_2d(&tm_q, q, kDQK, (uint64_t)bd.total_q * kH, 64, kH)) return cudaErrorInvalidValue;
     cudaError_t e =
-        cudaFuncSetAttribute(sparse_mla_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(rows_per_seq * splits), bd.B);
-    sparse_mla_simt_kernel<<<grid, kThreads, smem, stream>>>(bd, rr, q, kv, idx, idx_local ? 1 : 0, k,
-                                                             rows_per_seq, splits, per_split, sm_scale, out,
-                                                             lse, part_o, part_lse, status);
+    sparse_mla_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(bd, rr, tm_q, kv, idx, idx_local ? 1 : 0, k,
+                                                                 rows_per_seq, splits, per_split, sm_scale, out,
+                                                                 lse, part_o, part_lse, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1);
