@@ -111,6 +111,10 @@ DSA_API dsa_status dsa_reset_device_status(void* ws, void* stream);
  * (DSA_OK if no kernel latched an error since the last reset). */
 DSA_API dsa_status dsa_read_device_status(const void* ws, void* stream, dsa_status* out);
 
+/* Text of the last CUDA error behind a DSA_ERR_CUDA returned to this host
+ * thread ("no error" if none).  Thread-local, static storage. */
+DSA_API const char* dsa_last_cuda_error(void);
+
 /* Number of kernels this library has launched in this process so far (all
  * devices, all streams).  Instrumentation for benchmarks; host only. */
 DSA_API uint64_t dsa_kernel_launch_count(void);

@@ -30,14 +30,17 @@ STATUS = {
     4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_BAD_BATCH", 7: "DSA_ERR_BAD_INDEX",
 }
 
-EXPORTS = ("dsa_status_string", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
+EXPORTS = ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
            "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward")
 
 
 class DsaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        msg = f"{where}: {STATUS.get(code, code)}"
+        if code == 4 and _lib is not None:
+            msg += f" ({_lib.dsa_last_cuda_error().decode()})"
+        super().__init__(msg)
 
 
 class DsaBatch(ctypes.Structure):
@@ -62,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     BP = ctypes.POINTER(DsaBatch)
     lib.dsa_status_string.restype = ctypes.c_char_p
     lib.dsa_status_string.argtypes = [i32]
+    lib.dsa_last_cuda_error.restype = ctypes.c_char_p
+    lib.dsa_last_cuda_error.argtypes = []
     lib.dsa_kernel_launch_count.restype = ctypes.c_uint64
     lib.dsa_kernel_launch_count.argtypes = []
     lib.dsa_workspace_size.argtypes = [BP, i32, ctypes.POINTER(sz)]
@@ -72,7 +77,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_sparse_mla_fwd.argtypes = [BP, P, P, P, i32, f32, P, P, P, sz, P]
     lib.dsa_forward.argtypes = [BP, P, P, P, P, P, i32, f32, P, P, P, P, i64, P, sz, P]
     for name in EXPORTS:
-        if name not in ("dsa_status_string", "dsa_kernel_launch_count"):
+        if name not in ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count"):
             getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib

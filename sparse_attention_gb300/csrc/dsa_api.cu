@@ -65,9 +65,12 @@ WsLayout ws_layout(const dsa_batch* b, int k) {
     return L;
 }
 
+thread_local cudaError_t t_last_error = cudaSuccess;
+
 dsa_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return DSA_OK;
-    cudaGetLastError();  // clear a sticky launch error of this thread
+    t_last_error = e;
+    cudaGetLastError();  // clear a non-sticky launch error of this thread
     return DSA_ERR_CUDA;
 }
 
@@ -97,6 +100,8 @@ const char* dsa_status_string(int s) {
         default: return "unknown dsa_status";
     }
 }
+
+const char* dsa_last_cuda_error(void) { return cudaGetErrorString(t_last_error); }
 
 uint64_t dsa_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -22,12 +22,14 @@
 //               128-byte row piece, coalesced) into nine 64-column chunks
 //               laid out 128B-swizzled; Q once by TMA
 //   warp 1      TMEM owner and MMA issuer
-//   warps 2..5  softmax: thread = one gathered row; the per-head block max
-//               is a warp max (redux.sync) plus a cross-warp max through
-//               shared memory; p = exp2(s*c - m) in fp32, written as bf16
-//               P^T over the RoPE chunk (no longer needed once S^T is
-//               done); O^T is rescaled in TMEM only when a head's running
-//               max grows by more than 2^8; final normalisation and store.
+//   warps 2..9  softmax: thread = one gathered row and 32 of the heads (two
+//               warps per TMEM lane quarter).  The running per-head max m
+//               only moves when some score exceeds it by more than 2^8 (a
+//               vote over the block); only then is the exact block max
+//               taken (warp max by redux.sync, then across lane quarters)
+//               and O^T rescaled in TMEM.  p = 2^(s*c - m) in fp32, written
+//               as bf16 P^T over the RoPE chunk (free once S^T is done);
+//               final normalisation and store.
 // A single 144 KiB row tile fits next to Q (72 KiB); it is refilled chunk
 // by chunk as soon as the MMAs that read each chunk have completed.
 // Split-K partials (for few query rows) are merged by merge_kernel.
@@ -47,7 +49,8 @@ constexpr int kChunks = kDQK / 64;           // 9 column chunks of 64
 constexpr int kVChunks = kDV / 64;           // the first 8 hold V
 constexpr int kKVChunkBytes = kBlk * 128;    // 16 KiB
 constexpr int kQChunkBytes = kH * 128;       // 8 KiB
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;                // producer, MMA, 8 softmax warps
+constexpr int kSoftmaxThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;         // rescale O only when a max grows by > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -79,11 +82,10 @@ constexpr uint32_t kTmemS = 256;                              // S^T: 64 columns
 
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_tc_kernel(const BatchDev bd, const RowRange rr, const __grid_constant__ CUtensorMap tm_q,
-                         const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
-                         const int idx_local, const int k, const int rows_per_seq, const int splits,
-                         const int per_split, const float sm_scale, uint16_t* __restrict__ out,
-                         float* __restrict__ lse, float* __restrict__ part_o, float* __restrict__ part_lse,
-                         int32_t* status) {
+                         const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx, const int idx_local,
+                         const int k, const int rows_per_seq, const int splits, const int per_split,
+                         const float sm_scale, uint16_t* __restrict__ out, float* __restrict__ lse,
+                         float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -98,7 +100,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* sel = idx + buf_row(idx_local, sq, b, i, rr) * (int64_t)k;
     const int j_begin = sp * per_split;
     const int j_end = min(k, j_begin + per_split);
-    const int32_t row0 = (int32_t)((int64_t)b * bd.stride);       // cache row of position 0
     const int64_t prow = ((int64_t)b * rows_per_seq + (i - rr.i0)) * splits + sp;   // split partial row
 
     const uint32_t sKV = smem_u32(smem + kOffKV);
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // blocks of this segment: up to its last valid entry
     if (warp == 0) {
         int last = -1;
+#pragma unroll 8
         for (int j = j_begin + (int)lane; j < j_end; j += 32)
             if (__ldg(sel + j) >= 0) last = j;
 #pragma unroll
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 0) {
         for (int n = 0; n < kNumBars; ++n) mbar_init(bar(n), 1);
-        mbar_init(bar(kBarP), 128);
+        mbar_init(bar(kBarP), kSoftmaxThreads);
         mbar_init(bar(kBarIdx), 32);
         mbar_init(bar(kBarIdx + 1), 32);
         for (int c = 0; c < kChunks; ++c) mbar_init(bar(kBarKV + c), 32);
@@ -154,7 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(sQ + c * kQChunkBytes, &tm_q, bar(kBarQ), c * 64, (int32_t)(grow * kH));
             }
         }
-        int issued = 0;
+        // lane (rq, piece): rows 4*n + rq of the block, 16-byte piece `piece`
+        // of each 128-byte row chunk; 8 lanes cover one row chunk (coalesced)
+        const int rq = (int)(lane >> 3), piece = (int)(lane & 7u);
+        const uint32_t dpat0 = (uint32_t)(rq * 128 + ((piece ^ rq) << 4));         // rows with r % 8 == rq
+        const uint32_t dpat1 = (uint32_t)(rq * 128 + ((piece ^ (rq + 4)) << 4));   // rows with r % 8 == rq + 4
+        const uint8_t* kv_seq = reinterpret_cast<const uint8_t*>(kv) + (int64_t)b * bd.stride * (kDQK * 2);
         for (int jb = 0; jb < nblk; ++jb) {
             const uint32_t ph = (uint32_t)jb & 1u;
             // indices of this block: validated, -1 where invalid or past the segment
@@ -162,12 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = j_begin + jb * kBlk + u * 32 + (int)lane;
-                int32_t s = (j < j_end) ? __ldg(sel + j) : -1;
-                if (s < -1 || s > t) {
+                int32_t sv = (j < j_end) ? __ldg(sel + j) : -1;
+                if (sv < -1 || sv > t) {
                     latch_status(status, DSA_ERR_BAD_INDEX);
-                    s = -1;
+                    sv = -1;
                 }
-                v[u] = s;
+                v[u] = sv;
             }
             // buffer jb & 1 was last read by the softmax of block jb - 2,
             // which finished before PV(jb - 1) started
@@ -183,8 +190,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 4; ++u) ib[u * 32 + lane] = v[u];
             __syncwarp();
             mbar_arrive(bar(kBarIdx + (jb & 1)));
-            const uint8_t* kv_seq = reinterpret_cast<const uint8_t*>(kv) + (int64_t)row0 * (kDQK * 2);
-            for (int c = 0; c < kChunks && ok; ++c) {
+            uint32_t soff[kBlk / 4];   // byte offset of each of this lane's rows (+ piece)
+#pragma unroll
+            for (int n = 0; n < kBlk / 4; ++n) {
+                const int32_t sv = ib[4 * n + rq];
+                soff[n] = (uint32_t)(sv >= 0 ? sv : 0) * (uint32_t)(kDQK * 2) + (uint32_t)(piece * 16);
+            }
+            for (int c = 0; c < kChunks; ++c) {
                 // chunk c of the previous block must have been consumed
                 if (jb > 0) {
                     const uint32_t fb = c < kVChunks ? bar(kBarPair + c / 2) : bar(kBarO);
@@ -192,20 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
-                // 4 rows x 8 pieces of 16 B per warp instruction
+                const uint8_t* src = kv_seq + c * 128;
                 const uint32_t dst = sKV + c * kKVChunkBytes;
-                const int piece = (int)(lane & 7u);
-#pragma unroll 4
-                for (int r4 = 0; r4 < kBlk; r4 += 4) {
-                    const int rr_ = r4 + (int)(lane >> 3);
-                    const int32_t s = ib[rr_];
-                    const uint8_t* src = kv_seq + (int64_t)(s >= 0 ? s : 0) * (kDQK * 2) + c * 128 + piece * 16;
-                    cp_async_16(dst + rr_ * 128 + ((piece ^ (rr_ & 7)) << 4), src);
-                }
+#pragma unroll
+                for (int n = 0; n < kBlk / 4; ++n)
+                    cp_async_16(dst + 512u * n + ((n & 1) ? dpat1 : dpat0), src + soff[n]);
                 cp_async_arrive(bar(kBarKV + c));
-                ++issued;
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) {
                 latch_status(status, DSA_ERR_TIMEOUT);
                 misc[1] = 1;
@@ -274,101 +279,115 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------------- softmax
-        const uint32_t lq = warp & 3u;                 // TMEM lane quarter
+        // warp w: TMEM lane quarter w % 4 (rows), head half (w - 2) / 4
+        const uint32_t lq = warp & 3u;
+        const int h0 = ((int)(warp - 2) >> 2) * 32;
         const int r = (int)(lq * 32 + lane);           // row of the block
-        const int st = (int)threadIdx.x - 64;          // 0..127 among the softmax threads
+        const int st = (int)threadIdx.x - 64;          // 0..255 among the softmax threads
         const uint32_t lane_base = (lq * 32u) << 16;
-        float lsum[kH];
+        float lsum[32];
 #pragma unroll
-        for (int h = 0; h < kH; ++h) lsum[h] = 0.f;
+        for (int x = 0; x < 32; ++x) lsum[x] = 0.f;
         bool ok = true;
         for (int jb = 0; jb < nblk; ++jb) {
             const uint32_t ph = (uint32_t)jb & 1u;
             const bool got = !misc[1] && mbar_wait(bar(kBarIdx + (jb & 1)), ((uint32_t)jb >> 1) & 1u) &&
                              mbar_wait(bar(kBarS), ph);
-            // every abort is agreed by all 128 softmax threads before any
-            // named barrier, so none of them can be left waiting at one
-            if (named_bar_or(3, 128, !got)) {
+            // every abort is agreed by all softmax threads before any named
+            // barrier, so none of them can be left waiting at one
+            if (named_bar_or(3, kSoftmaxThreads, !got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const bool valid = s_idx[(jb & 1) * kBlk + r] >= 0;
-            float s[kH];
+            float s[32];
             {
                 uint32_t u[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kTmemS, u);
+                tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + h0, u);
                 tmem_ld_wait();
 #pragma unroll
-                for (int h = 0; h < 32; ++h) s[h] = valid ? __uint_as_float(u[h]) : -INFINITY;
-                tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + 32, u);
-                tmem_ld_wait();
-#pragma unroll
-                for (int h = 0; h < 32; ++h) s[32 + h] = valid ? __uint_as_float(u[h]) : -INFINITY;
+                for (int x = 0; x < 32; ++x) s[x] = valid ? __uint_as_float(u[x]) : -INFINITY;
             }
-            // per-head block max: a warp max, then across the four warps
+            // the running max moves only when a score exceeds it by 2^8
+            bool exceed = false;
 #pragma unroll
-            for (int h = 0; h < kH; ++h) {
-                const float m = warp_max_f32(s[h]);
-                if (lane == 0) s_wmax[lq * kH + h] = m;
+            for (int x = 0; x < 32; x += 4) {
+                const float4 mv = *reinterpret_cast<const float4*>(s_m + h0 + x);
+                exceed |= s[x] * c2 > mv.x + kRescaleLog2;
+                exceed |= s[x + 1] * c2 > mv.y + kRescaleLog2;
+                exceed |= s[x + 2] * c2 > mv.z + kRescaleLog2;
+                exceed |= s[x + 3] * c2 > mv.w + kRescaleLog2;
             }
-            named_bar_sync(1, 128);
-            bool need = false;
-            if (st < kH) {
-                const float mb =
-                    fmaxf(fmaxf(s_wmax[st], s_wmax[kH + st]), fmaxf(s_wmax[2 * kH + st], s_wmax[3 * kH + st]));
-                const float mold = s_m[st];
-                const float mnew = mb * c2;
-                float alpha = 1.f;
-                if (mb > -INFINITY && (mold == -INFINITY || mnew > mold + kRescaleLog2)) {
-                    alpha = exp2f(mold - mnew);              // 0 when nothing was seen yet
-                    s_m[st] = mnew;
-                    need = true;
+            if (named_bar_or(2, kSoftmaxThreads, exceed)) {
+                // exact per-head block max: warp max, then across lane quarters
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const float mx = warp_max_f32(s[x]);
+                    if (lane == 0) s_wmax[lq * kH + h0 + x] = mx;
                 }
-                s_alpha[st] = alpha;
-            }
-            const bool rescale = named_bar_or(2, 128, need);
-            if (rescale) {
-                // O^T holds the blocks before jb once PV(jb - 1) has completed
-                const bool w = jb == 0 || mbar_wait(bar(kBarO), ph ^ 1u);
-                if (named_bar_or(3, 128, !w)) {
-                    ok = false;
-                    break;
-                }
-                if (jb > 0) {
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int cb = 0; cb < 8; ++cb) {
-                        uint32_t u[32];
-                        const uint32_t ta = tmem + lane_base + kTmemO + cb * 32;
-                        tmem_ld_32x32b_x32(ta, u);
-                        tmem_ld_wait();
-                        const float* al = s_alpha + (cb & 1) * 32;
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * al[x]);
-                        tmem_st_32x32b_x32(ta, u);
+                named_bar_sync(1, kSoftmaxThreads);
+                bool need = false;
+                if (st < kH) {
+                    const float mb = fmaxf(fmaxf(s_wmax[st], s_wmax[kH + st]),
+                                           fmaxf(s_wmax[2 * kH + st], s_wmax[3 * kH + st]));
+                    const float mold = s_m[st];
+                    const float mnew = mb * c2;
+                    float alpha = 1.f;
+                    if (mb > -INFINITY && (mold == -INFINITY || mnew > mold + kRescaleLog2)) {
+                        alpha = exp2f(mold - mnew);          // 0 when nothing was seen yet
+                        s_m[st] = mnew;
+                        need = true;
                     }
-                    tmem_st_wait();
+                    s_alpha[st] = alpha;
                 }
+                if (named_bar_or(2, kSoftmaxThreads, need)) {
+                    // O^T holds the blocks before jb once PV(jb - 1) has completed
+                    const bool w = jb == 0 || mbar_wait(bar(kBarO), ph ^ 1u);
+                    if (named_bar_or(3, kSoftmaxThreads, !w)) {
+                        ok = false;
+                        break;
+                    }
+                    if (jb > 0) {
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int piece = 0; piece < 8; ++piece) {      // 4 dv blocks x 2 halves
+                            uint32_t u[16];
+                            const int hx = (piece & 1) * 16;
+                            const uint32_t ta = tmem + lane_base + kTmemO + (piece >> 1) * kH + h0 + hx;
+                            tmem_ld_32x32b_x16(ta, u);
+                            tmem_ld_wait();
 #pragma unroll
-                for (int h = 0; h < kH; ++h) lsum[h] *= s_alpha[h];
+                            for (int x = 0; x < 16; ++x)
+                                u[x] = __float_as_uint(__uint_as_float(u[x]) * s_alpha[h0 + hx + x]);
+                            tmem_st_32x32b_x16(ta, u);
+                        }
+                        tmem_st_wait();
+                    }
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) lsum[x] *= s_alpha[h0 + x];
+                }
             }
-            // P^T row r over the RoPE chunk, 128B-swizzled (MN-major B operand)
+            // P^T row r, heads h0..h0+31: 4 swizzled 16-byte pieces (MN-major B)
             uint8_t* prow = smem + kOffKV + kVChunks * kKVChunkBytes + r * 128;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int e4 = 0; e4 < 4; ++e4) {
+                const float4 ma = *reinterpret_cast<const float4*>(s_m + h0 + e4 * 8);
+                const float4 mb = *reinterpret_cast<const float4*>(s_m + h0 + e4 * 8 + 4);
+                const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
                 float p[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int h = c8 * 8 + e;
-                    p[e] = valid ? exp2f(fmaf(s[h], c2, -s_m[h])) : 0.f;
-                    lsum[h] += p[e];
+                    const int x = e4 * 8 + e;
+                    p[e] = valid ? ex2_approx(fmaf(s[x], c2, -mm[e])) : 0.f;
+                    lsum[x] += p[e];
                 }
                 uint4 pk;
                 pk.x = pack_bf16x2(p[0], p[1]);
                 pk.y = pack_bf16x2(p[2], p[3]);
                 pk.z = pack_bf16x2(p[4], p[5]);
                 pk.w = pack_bf16x2(p[6], p[7]);
+                const int c8 = (h0 >> 3) + e4;
                 *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = pk;
             }
             fence_proxy_async_smem();
@@ -382,15 +401,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- epilogue
         // l: the per-thread partial sums reduced over the 128 rows
 #pragma unroll
-        for (int h = 0; h < kH; ++h) {
-            float v = lsum[h];
+        for (int x = 0; x < 32; ++x) {
+            float v = lsum[x];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) s_l[lq * kH + h] = v;
+            if (lane == 0) s_l[lq * kH + h0 + x] = v;
         }
         bool w = ok && (nblk == 0 || mbar_wait(bar(kBarO), ((uint32_t)nblk - 1u) & 1u));
         w = __all_sync(0xffffffffu, w);
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kSoftmaxThreads);
         if (st < kH) {
             const float lt = s_l[st] + s_l[kH + st] + s_l[2 * kH + st] + s_l[3 * kH + st];
             s_l[4 * kH + st] = lt;
@@ -401,33 +420,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 part_lse[prow * kH + st] = ls;
             }
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kSoftmaxThreads);
         if (w) {
             tc_fence_after();
-            const float* lt = s_l + 4 * kH;
+            const float* lt = s_l + 4 * kH + h0;
             for (int dv = 0; dv < 4; ++dv) {
                 const int d = dv * 128 + r;                   // output column of this thread
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t u[32];
-                    if (nblk > 0) {
-                        tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + dv * kH + half * 32, u);
-                        tmem_ld_wait();
+                uint32_t u[32];
+                if (nblk > 0) {
+                    tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + dv * kH + h0, u);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) u[x] = 0u;
+                }
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const int h = h0 + x;
+                    const float l = lt[x];
+                    const float o = l > 0.f ? __uint_as_float(u[x]) / l : 0.f;
+                    if (splits == 1) {
+                        const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+                        out[(grow * kH + h) * kDV + d] = *reinterpret_cast<const uint16_t*>(&ob);
                     } else {
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) u[x] = 0u;
-                    }
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        const int h = half * 32 + x;
-                        const float l = lt[h];
-                        const float o = l > 0.f ? __uint_as_float(u[x]) / l : 0.f;
-                        if (splits == 1) {
-                            const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-                            out[(grow * kH + h) * kDV + d] = *reinterpret_cast<const uint16_t*>(&ob);
-                        } else {
-                            part_o[(prow * kH + h) * kDV + d] = o;
-                        }
+                        part_o[(prow * kH + h) * kDV + d] = o;
                     }
                 }
             }
