@@ -17,12 +17,13 @@
 //   O^T[512, 64]           += V_blk^T[512, 128] . P^T[128, 64]  (MN-major A and B)
 // V_blk is the first 512 columns of the same gathered tile, so every row is
 // read from memory once.  Roles by warp:
-//   warp 0      producer: validates the block's indices and gathers the
+//   warps 0, 1  producers: validate the block's indices and gather the
 //               576-wide rows with 16-byte cp.async copies (8 lanes per
-//               128-byte row piece, coalesced) into nine 64-column chunks
-//               laid out 128B-swizzled; Q once by TMA
-//   warp 1      TMEM owner and MMA issuer
-//   warps 2..9  softmax: thread = one gathered row and 32 of the heads (two
+//               128-byte row piece, coalesced; 8 rows per instruction pair)
+//               into nine 64-column chunks laid out 128B-swizzled; Q once
+//               by TMA
+//   warp 2      TMEM owner and MMA issuer
+//   warps 3..10 softmax: thread = one gathered row and 32 of the heads (two
 //               warps per TMEM lane quarter).  The running per-head max m
 //               only moves when some score exceeds it by more than 2^8 (a
 //               vote over the block); only then is the exact block max
@@ -49,8 +50,11 @@ constexpr int kChunks = kDQK / 64;           // 9 column chunks of 64
 constexpr int kVChunks = kDV / 64;           // the first 8 hold V
 constexpr int kKVChunkBytes = kBlk * 128;    // 16 KiB
 constexpr int kQChunkBytes = kH * 128;       // 8 KiB
-constexpr int kThreads = 320;                // producer, MMA, 8 softmax warps
+constexpr int kProducerWarps = 2;
+constexpr int kMmaWarp = kProducerWarps;                  // warp 2
+constexpr int kSoftmaxWarp0 = kMmaWarp + 1;               // warps 3..10
 constexpr int kSoftmaxThreads = 256;
+constexpr int kThreads = 32 * kSoftmaxWarp0 + kSoftmaxThreads;   // 352
 constexpr float kRescaleLog2 = 8.0f;         // rescale O only when a max grows by > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -129,15 +133,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kBarP), kSoftmaxThreads);
         mbar_init(bar(kBarIdx), 32);
         mbar_init(bar(kBarIdx + 1), 32);
-        for (int c = 0; c < kChunks; ++c) mbar_init(bar(kBarKV + c), 32);
+        for (int c = 0; c < kChunks; ++c) mbar_init(bar(kBarKV + c), 32 * kProducerWarps);
         misc[1] = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
         tmem_relinquish();
     }
-    if (threadIdx.x >= 64 && threadIdx.x < 64 + kH) s_m[threadIdx.x - 64] = -INFINITY;
+    if (threadIdx.x >= 32 * kSoftmaxWarp0 && threadIdx.x < 32 * kSoftmaxWarp0 + kH)
+        s_m[threadIdx.x - 32 * kSoftmaxWarp0] = -INFINITY;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -145,9 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nblk = (int)misc[2];
     const float c2 = sm_scale * kLog2e;      // logits in log2 units
 
-    if (warp == 0) {
-        // ----------------------------------------------------------- producer
-        const bool leader = lane == 0;
+    if (warp < kProducerWarps) {
+        // ----------------------------------------------------------- producers
+        const bool leader = threadIdx.x == 0;
         if (leader) {
             prefetch_tmap(&tm_q);
             if (nblk > 0) {
@@ -156,44 +161,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(sQ + c * kQChunkBytes, &tm_q, bar(kBarQ), c * 64, (int32_t)(grow * kH));
             }
         }
-        // lane (rq, piece): rows 4*n + rq of the block, 16-byte piece `piece`
-        // of each 128-byte row chunk; 8 lanes cover one row chunk (coalesced)
-        const int rq = (int)(lane >> 3), piece = (int)(lane & 7u);
-        const uint32_t dpat0 = (uint32_t)(rq * 128 + ((piece ^ rq) << 4));         // rows with r % 8 == rq
-        const uint32_t dpat1 = (uint32_t)(rq * 128 + ((piece ^ (rq + 4)) << 4));   // rows with r % 8 == rq + 4
+        // producer lane gl = (rq, piece): rows 8n + rq of the block, 16-byte
+        // piece `piece` of each 128-byte row chunk; 8 lanes cover one row
+        // chunk (coalesced) and row r % 8 == rq fixes the swizzle
+        const int gl = (int)threadIdx.x;
+        const int rq = gl >> 3, piece = gl & 7;
+        const uint32_t dpat = (uint32_t)(rq * 128 + ((piece ^ rq) << 4));
         const uint8_t* kv_seq = reinterpret_cast<const uint8_t*>(kv) + (int64_t)b * bd.stride * (kDQK * 2);
+        bool ok = true;
         for (int jb = 0; jb < nblk; ++jb) {
             const uint32_t ph = (uint32_t)jb & 1u;
-            // indices of this block: validated, -1 where invalid or past the segment
-            int32_t v[4];
+            int32_t* ib = s_idx + (jb & 1) * kBlk;
+            if (warp == 0) {
+                // indices of this block: validated, -1 where invalid or past the segment
+                int32_t v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = j_begin + jb * kBlk + u * 32 + (int)lane;
-                int32_t sv = (j < j_end) ? __ldg(sel + j) : -1;
-                if (sv < -1 || sv > t) {
-                    latch_status(status, DSA_ERR_BAD_INDEX);
-                    sv = -1;
+                for (int u = 0; u < 4; ++u) {
+                    const int j = j_begin + jb * kBlk + u * 32 + (int)lane;
+                    int32_t sv = (j < j_end) ? __ldg(sel + j) : -1;
+                    if (sv < -1 || sv > t) {
+                        latch_status(status, DSA_ERR_BAD_INDEX);
+                        sv = -1;
+                    }
+                    v[u] = sv;
                 }
-                v[u] = sv;
+                // buffer jb & 1 was last read by the softmax of block jb - 2,
+                // which finished before PV(jb - 1) started
+                ok = jb == 0 || (!misc[1] && mbar_wait(bar(kBarPair), ph ^ 1u));
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) ib[u * 32 + lane] = v[u];
+                    __syncwarp();
+                    mbar_arrive(bar(kBarIdx + (jb & 1)));
+                } else {
+                    misc[1] = 1;
+                }
             }
-            // buffer jb & 1 was last read by the softmax of block jb - 2,
-            // which finished before PV(jb - 1) started
-            bool ok = jb == 0 || (!misc[1] && mbar_wait(bar(kBarPair), ph ^ 1u));
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                latch_status(status, DSA_ERR_TIMEOUT);
-                misc[1] = 1;
+            named_bar_sync(4, 32 * kProducerWarps);     // the block's indices are in shared memory
+            if (misc[1]) {
+                ok = false;
                 break;
             }
-            int32_t* ib = s_idx + (jb & 1) * kBlk;
+            uint32_t soff[kBlk / 8];   // byte offset of each of this lane's rows (+ piece)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) ib[u * 32 + lane] = v[u];
-            __syncwarp();
-            mbar_arrive(bar(kBarIdx + (jb & 1)));
-            uint32_t soff[kBlk / 4];   // byte offset of each of this lane's rows (+ piece)
-#pragma unroll
-            for (int n = 0; n < kBlk / 4; ++n) {
-                const int32_t sv = ib[4 * n + rq];
+            for (int n = 0; n < kBlk / 8; ++n) {
+                const int32_t sv = ib[8 * n + rq];
                 soff[n] = (uint32_t)(sv >= 0 ? sv : 0) * (uint32_t)(kDQK * 2) + (uint32_t)(piece * 16);
             }
             for (int c = 0; c < kChunks; ++c) {
@@ -205,25 +218,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                 }
                 const uint8_t* src = kv_seq + c * 128;
-                const uint32_t dst = sKV + c * kKVChunkBytes;
+                const uint32_t dst = sKV + c * kKVChunkBytes + dpat;
 #pragma unroll
-                for (int n = 0; n < kBlk / 4; ++n)
-                    cp_async_16(dst + 512u * n + ((n & 1) ? dpat1 : dpat0), src + soff[n]);
+                for (int n = 0; n < kBlk / 8; ++n) cp_async_16(dst + 1024u * n, src + soff[n]);
                 cp_async_arrive(bar(kBarKV + c));
             }
-            if (!ok) {
-                latch_status(status, DSA_ERR_TIMEOUT);
+            // both producer warps agree before either starts the next block
+            if (named_bar_or(5, 32 * kProducerWarps, !ok)) {
+                ok = false;
                 misc[1] = 1;
                 break;
             }
         }
+        if (!ok) latch_status(status, DSA_ERR_TIMEOUT);
         if (misc[1]) {
             // wind down: let every copy this warp started land first
             asm volatile("cp.async.wait_all;" ::: "memory");
             if (leader && nblk > 0) mbar_wait(bar(kBarQ), 0);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA
         if (elect_one()) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kH, false, false);
@@ -279,11 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------------- softmax
-        // warp w: TMEM lane quarter w % 4 (rows), head half (w - 2) / 4
+        // warp w: TMEM lane quarter w % 4 (rows), head half (w - 3) / 4
         const uint32_t lq = warp & 3u;
-        const int h0 = ((int)(warp - 2) >> 2) * 32;
+        const int h0 = ((int)(warp - kSoftmaxWarp0) >> 2) * 32;
         const int r = (int)(lq * 32 + lane);           // row of the block
-        const int st = (int)threadIdx.x - 64;          // 0..255 among the softmax threads
+        const int st = (int)threadIdx.x - 32 * kSoftmaxWarp0;   // 0..255 among the softmax threads
         const uint32_t lane_base = (lq * 32u) << 16;
         float lsum[32];
 #pragma unroll
@@ -452,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -505,13 +519,23 @@ __global__ void __launch_bounds__(256)
     if (lse && part == 0) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
-// CTAs per query row: about one CTA per SM in total (one CTA fills an SM's
-// shared memory), at least one 128-row block each.
+// CTAs per query row.  One CTA fills an SM's shared memory, so the grid
+// runs in waves of kNumSMs CTAs; pick the split count that minimises
+// waves x (blocks per CTA + one block's worth of per-CTA overhead).
 int choose_splits(int64_t rows, int k) {
     if (rows <= 0) return 1;
-    const int64_t want = (kNumSMs + rows - 1) / rows;
-    const int max_by_k = std::max(1, (k + kBlk - 1) / kBlk);
-    return (int)std::min<int64_t>(std::max<int64_t>(1, want), std::min(16, max_by_k));
+    const int nblk = std::max(1, (k + kBlk - 1) / kBlk);
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int sp = 1; sp <= std::min(16, nblk); ++sp) {
+        const int64_t waves = (rows * sp + kNumSMs - 1) / kNumSMs;
+        const int64_t cost = waves * ((nblk + sp - 1) / sp + 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = sp;
+        }
+    }
+    return best;
 }
 
 }  // namespace
