@@ -152,6 +152,35 @@ DSA_API dsa_status dsa_sparse_mla_fwd(const dsa_batch* batch, const uint16_t* q,
                               const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* Step 3 for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call; it exists for integration.  Some callers cannot
+ * allocate at the point where attention runs: code inside a CUDA stream
+ * capture that must not allocate, serving loops that budget every byte of
+ * device memory in advance and treat any allocation as a failure, or
+ * embedders whose allocator is not reachable from the calling thread.  This
+ * call computes exactly what dsa_sparse_mla_fwd computes (same kernels, same
+ * split of each query's selected list, so the same bits), but it takes no
+ * workspace: its split-K partials live in a 32 MiB array of static device
+ * memory owned by the library, which every GPU that loads the library holds
+ * until the process exits.  It calls no cudaMalloc or cudaFree.
+ *   device_status  optional DEVICE int32 (caller-owned, cleared by the
+ *                  caller); device-side errors (indices outside [-1, t], a
+ *                  batch outside its bounds) are latched there; NULL = not
+ *                  reported.
+ * Returns DSA_ERR_WORKSPACE, before launching anything, when the call's
+ * partials would not fit in the 32 MiB array: each partial (one split of one
+ * query row) takes 131,328 bytes, so at most 255 fit.  Decode batches fit
+ * (64 rows x 2 splits or 8 rows x 16 splits: 16.8 MB); large batches that
+ * still split their rows (e.g. 1140 rows at k = 2047) do not.
+ * The first call on a device looks up the array's device address (once per
+ * device); make that first call before any stream capture.  Every call on a
+ * device shares the one array, so calls whose kernels overlap on the GPU
+ * (different streams, or different host threads) race and corrupt each
+ * other's results: order them on one stream. */
+DSA_API dsa_status dsa_sparse_mla_fwd_noalloc(const dsa_batch* batch, const uint16_t* q, const uint16_t* kv,
+                                              const int32_t* idx, int k, float sm_scale, uint16_t* out,
+                                              float* lse, int32_t* device_status, void* stream);
+
 /* Steps 1-3 in one call (prefill, one chunk of a chunked prefill, or a
  * decode step).  idx_out [total_q, k] and scores_out [total_q, ld] are
  * optional (NULL = keep them in the workspace only); ld is ignored when

@@ -31,7 +31,7 @@ STATUS = {
 }
 
 EXPORTS = ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
-           "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward")
+           "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd", "dsa_sparse_mla_fwd_noalloc", "dsa_forward")
 
 
 class DsaError(RuntimeError):
@@ -75,6 +75,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_indexer_scores.argtypes = [BP, P, P, P, P, i64, P, sz, P]
     lib.dsa_topk.argtypes = [BP, P, i64, i32, P, P, sz, P]
     lib.dsa_sparse_mla_fwd.argtypes = [BP, P, P, P, i32, f32, P, P, P, sz, P]
+    lib.dsa_sparse_mla_fwd_noalloc.argtypes = [BP, P, P, P, i32, f32, P, P, P, P]
     lib.dsa_forward.argtypes = [BP, P, P, P, P, P, i32, f32, P, P, P, P, i64, P, sz, P]
     for name in EXPORTS:
         if name not in ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count"):
@@ -199,6 +200,20 @@ def sparse_mla_fwd(batch: Batch, q, kv, idx, k: int, sm_scale: float, out, lse=N
                                              float(sm_scale), _bf16(out), _p(lse), _p(ws),
                                              ws.numel() if ws is not None else 0, _stream(stream)),
            "dsa_sparse_mla_fwd")
+    return out
+
+
+def sparse_mla_fwd_noalloc(batch: Batch, q, kv, idx, k: int, sm_scale: float, out, lse=None, device_status=None,
+                           stream=None):
+    """dsa_sparse_mla_fwd without a workspace: the split-K partials live in
+    the library's static device scratch (for callers that cannot allocate).
+    Calls that overlap on the GPU race; the first call on a device should
+    come before any stream capture."""
+    assert idx.dtype == torch.int32 and (lse is None or lse.dtype == torch.float32)
+    assert device_status is None or device_status.dtype == torch.int32
+    _check(load_library().dsa_sparse_mla_fwd_noalloc(ctypes.byref(batch.c), _bf16(q), _bf16(kv), _p(idx), int(k),
+                                                     float(sm_scale), _bf16(out), _p(lse), _p(device_status),
+                                                     _stream(stream)), "dsa_sparse_mla_fwd_noalloc")
     return out
 
 
