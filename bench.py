@@ -291,6 +291,7 @@ def host_sample(case: Case, n_seq: int):
 
     if wl.kind == "decode":
         ctx = wl.ctx
+        n_seq = min(n_seq, wl.B)
         rows = slice(0, n_seq)
         cache = slice(0, n_seq * bt.stride)
         b = W.Batch(B=n_seq, stride=bt.stride, q_off=np.arange(n_seq + 1, dtype=np.int32),
@@ -302,7 +303,7 @@ def host_sample(case: Case, n_seq: int):
     b = W.Batch(B=1, stride=bt.stride, q_off=np.array([0, T], np.int32), ctx_len=np.array([T], np.int32),
                 q_idx=bits(bt.q_idx), w=bt.w.cpu().numpy(), k_idx=bits(bt.k_idx), q=bits(bt.q), kv=bits(bt.kv),
                 k=wl.k, sm_scale=bt.sm_scale)
-    rows = sorted(set(int(x) for x in np.linspace(0, T - 1, n_seq)))
+    rows = sorted(set(int(x) for x in np.linspace(0, T - 1, min(n_seq, T))))
     return b, rows, len(rows), f"{len(rows)} evenly spaced query rows of the {T}-token prefill"
 
 

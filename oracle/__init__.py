@@ -86,7 +86,28 @@ def _np(x, dtype) -> np.ndarray:
 def _rows(batch, rows: Optional[Sequence[int]]) -> np.ndarray:
     if rows is None:
         rows = range(batch.total_q)
-    return np.ascontiguousarray(np.asarray(list(rows), dtype=np.int32))
+    r = np.ascontiguousarray(np.asarray(list(rows), dtype=np.int32))
+    if len(r) and (r.min() < 0 or r.max() >= batch.total_q):
+        raise ValueError("row index outside the batch")
+    return r
+
+
+def _check_layout(batch, **arrays) -> None:
+    """Refuse a batch description larger than the arrays it points into, so
+    that the C code can never read past them."""
+    q_off = np.asarray(_np(batch.q_off, np.int32))
+    ctx = np.asarray(_np(batch.ctx_len, np.int32))
+    if len(q_off) != batch.B + 1 or len(ctx) != batch.B or q_off[0] != 0:
+        raise ValueError("q_off / ctx_len do not match B")
+    nq = np.diff(q_off)
+    if np.any(nq < 0) or np.any(nq > ctx) or np.any(ctx > batch.stride) or int(q_off[-1]) != batch.total_q:
+        raise ValueError("inconsistent batch layout")
+    need = {"q_idx": batch.total_q * H_IDX * D_IDX, "w": batch.total_q * H_IDX,
+            "k_idx": batch.B * batch.stride * D_IDX, "q": batch.total_q * H * D_QK,
+            "kv": batch.B * batch.stride * D_QK}
+    for name, a in arrays.items():
+        if a.size < need[name]:
+            raise ValueError(f"{name} holds {a.size} elements, the batch needs {need[name]}")
 
 
 def num_threads() -> int:
@@ -105,6 +126,7 @@ def indexer_scores(batch, rows: Optional[Sequence[int]] = None, ld: Optional[int
     out = np.full((len(r), ld), np.nan, dtype=np.float64)
     q_off, ctx = _np(batch.q_off, np.int32), _np(batch.ctx_len, np.int32)
     qi, w, ki = _np(batch.q_idx, np.uint16), _np(batch.w, np.float32), _np(batch.k_idx, np.uint16)
+    _check_layout(batch, q_idx=qi, w=w, k_idx=ki)
     lib.oracle_indexer_scores(batch.B, _ptr(q_off), _ptr(ctx), int(batch.stride), _ptr(qi), _ptr(w),
                               _ptr(ki), len(r), _ptr(r), _ptr(out), ld)
     return out
@@ -119,6 +141,11 @@ def topk(batch, scores: np.ndarray, rows: Optional[Sequence[int]] = None, k: Opt
     assert s.ndim == 2 and s.shape[0] == len(r)
     out = np.empty((len(r), k), dtype=np.int32)
     q_off, ctx = _np(batch.q_off, np.int32), _np(batch.ctx_len, np.int32)
+    _check_layout(batch)
+    pos = ctx[np.searchsorted(q_off, r, side="right") - 1] - np.diff(q_off)[np.searchsorted(q_off, r, side="right") - 1] \
+        + (r - q_off[np.searchsorted(q_off, r, side="right") - 1])
+    if len(r) and int(pos.max()) + 1 > s.shape[1]:
+        raise ValueError("score rows shorter than the positions they cover")
     lib.oracle_topk(batch.B, _ptr(q_off), _ptr(ctx), _ptr(s), s.shape[1], len(r), _ptr(r), k, _ptr(out))
     return out
 
@@ -132,6 +159,9 @@ def _mla(fn, batch, idx, rows, sm_scale) -> Tuple[np.ndarray, np.ndarray]:
     lse = np.empty((len(r), H), dtype=np.float64)
     q_off, ctx = _np(batch.q_off, np.int32), _np(batch.ctx_len, np.int32)
     q, kv = _np(batch.q, np.uint16), _np(batch.kv, np.uint16)
+    _check_layout(batch, q=q, kv=kv)
+    if idx.size and int(idx.max()) >= batch.stride:
+        raise ValueError("index outside the cache")
     scale = float(sm_scale if sm_scale is not None else batch.sm_scale)
     fn(batch.B, _ptr(q_off), _ptr(ctx), int(batch.stride), _ptr(q), _ptr(kv), _ptr(idx), k, scale,
        len(r), _ptr(r), _ptr(out), _ptr(lse))

@@ -307,3 +307,18 @@ def test_attention_full_path_on_tiny_prefill_is_dense_below_k():
     od, _ = oracle.masked_mla(batch, dense_idx)
     np.testing.assert_allclose(o[:16], od[:16], rtol=1e-11, atol=1e-13)
     assert not np.allclose(o[30:], od[30:])
+
+
+def test_oracle_wrapper_refuses_batches_larger_than_their_arrays():
+    # a batch description naming more sequences than the arrays hold must be
+    # refused before the C code runs (it would read past the arrays)
+    small = W.make_batch_np([16], [1], k=4, seed=61)
+    big = W.Batch(B=3, stride=16, q_off=np.arange(4, dtype=np.int32), ctx_len=np.full(3, 16, np.int32),
+                  q_idx=small.q_idx, w=small.w, k_idx=small.k_idx, q=small.q, kv=small.kv, k=4,
+                  sm_scale=W.SM_SCALE)
+    with pytest.raises(ValueError):
+        oracle.indexer_scores(big)
+    with pytest.raises(ValueError):
+        oracle.sparse_mla(big, np.zeros((3, 4), np.int32))
+    with pytest.raises(ValueError):
+        oracle.topk(small, np.zeros((1, 8), np.float32), k=4)     # row shorter than t + 1 = 16
