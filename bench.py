@@ -179,8 +179,9 @@ class Case:
                     topk_bytes=topk_bytes)
 
     def kernel_times_us(self, reps: int):
-        """Average device time of each step call (indexer, top-k, attention)
-        with CUDA events on the launching stream."""
+        """Average device time of each step call (indexer, top-k, attention):
+        `reps` back-to-back calls between two CUDA events on the launching
+        stream, so host submission overlaps the device work."""
         import torch
         dsa, wl = self.dsa, self.wl
         stream = torch.cuda.current_stream()
@@ -190,22 +191,24 @@ class Case:
         ld = (b.max_ctx + 3) // 4 * 4
         scores = torch.empty((b.total_q, ld), dtype=torch.float32, device=self.dev)
         idx = torch.empty((b.total_q, wl.k), dtype=torch.int32, device=self.dev)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        tot = [0.0, 0.0, 0.0]
-        for r in range(reps + 2):
-            ev[0].record(stream)
-            dsa.indexer_scores(b, q_idx, w, self.bt.k_idx, scores, ld=ld, ws=self.ws[j])
-            ev[1].record(stream)
-            dsa.topk(b, scores, wl.k, idx, ld=ld, ws=self.ws[j])
-            ev[2].record(stream)
-            dsa.sparse_mla_fwd(b, q, self.bt.kv, idx, wl.k, self.bt.sm_scale, self.out[:b.total_q],
-                               self.lse[:b.total_q], ws=self.ws[j])
-            ev[3].record(stream)
+        calls = {
+            "indexer": lambda: dsa.indexer_scores(b, q_idx, w, self.bt.k_idx, scores, ld=ld, ws=self.ws[j]),
+            "topk": lambda: dsa.topk(b, scores, wl.k, idx, ld=ld, ws=self.ws[j]),
+            "sparse_mla": lambda: dsa.sparse_mla_fwd(b, q, self.bt.kv, idx, wl.k, self.bt.sm_scale,
+                                                     self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j]),
+        }
+        times = {}
+        for name, fn in calls.items():
+            fn()
             torch.cuda.synchronize()
-            if r >= 2:
-                for x in range(3):
-                    tot[x] += ev[x].elapsed_time(ev[x + 1]) * 1e3
-        return {"indexer": tot[0] / reps, "topk": tot[1] / reps, "sparse_mla": tot[2] / reps}
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[name] = e0.elapsed_time(e1) * 1e3 / reps
+        return times
 
     def kernel_work_one_call(self):
         """Algorithmic work of the calls timed by kernel_times_us (call 0)."""

@@ -472,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// out = sum_s exp(lse_s - L) * o_s, L = log sum_s exp(lse_s)
+// out = sum_s exp(lse_s - L) * o_s, L = log sum_s exp(lse_s).  One CTA per
+// (query row, 8 heads); warp = head, lane = 16 output columns.
 __global__ void __launch_bounds__(256)
     merge_kernel(const BatchDev bd, const RowRange rr, const int rows_per_seq, const int splits,
                  const float* __restrict__ part_o, const float* __restrict__ part_lse, uint16_t* __restrict__ out,
@@ -480,26 +481,27 @@ __global__ void __launch_bounds__(256)
     const int b = blockIdx.y;
     SeqInfo sq;
     if (!load_seq(bd, b, status, sq)) return;
-    const int32_t i = rr.i0 + (int32_t)blockIdx.x;
+    const int32_t i = rr.i0 + (int32_t)(blockIdx.x >> 3);
     if (i >= min(rr.i1, sq.nq)) return;
     const int64_t grow = (int64_t)sq.q0 + i;
     const int64_t prow0 = ((int64_t)b * rows_per_seq + (i - rr.i0)) * splits;
-    const int h = threadIdx.x >> 2, part = threadIdx.x & 3;   // 64 heads x 4 column quarters
+    const int h = (int)(blockIdx.x & 7) * 8 + (int)(threadIdx.x >> 5);
+    const int c0 = (int)(threadIdx.x & 31) * 16;
     float mx = -INFINITY;
     for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[(prow0 + s) * kH + h]);
     float wsum = 0.f;
-    float acc[128];
+    float acc[16];
 #pragma unroll
-    for (int c = 0; c < 128; ++c) acc[c] = 0.f;
+    for (int c = 0; c < 16; ++c) acc[c] = 0.f;
     if (mx > -INFINITY) {
         for (int s = 0; s < splits; ++s) {
             const float ls = part_lse[(prow0 + s) * kH + h];
             if (ls == -INFINITY) continue;
             const float wgt = expf(ls - mx);
             wsum += wgt;
-            const float4* o = reinterpret_cast<const float4*>(part_o + ((prow0 + s) * kH + h) * kDV + part * 128);
+            const float4* o = reinterpret_cast<const float4*>(part_o + ((prow0 + s) * kH + h) * kDV + c0);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 const float4 v = o[c];
                 acc[4 * c] = fmaf(wgt, v.x, acc[4 * c]);
                 acc[4 * c + 1] = fmaf(wgt, v.y, acc[4 * c + 1]);
@@ -509,14 +511,17 @@ __global__ void __launch_bounds__(256)
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint2* o = reinterpret_cast<uint2*>(out + (grow * kH + h) * kDV + part * 128);
+    uint4* o = reinterpret_cast<uint4*>(out + (grow * kH + h) * kDV + c0);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        const __nv_bfloat162 v0 = __floats2bfloat162_rn(acc[4 * c] * inv, acc[4 * c + 1] * inv);
-        const __nv_bfloat162 v1 = __floats2bfloat162_rn(acc[4 * c + 2] * inv, acc[4 * c + 3] * inv);
-        o[c] = make_uint2(*reinterpret_cast<const uint32_t*>(&v0), *reinterpret_cast<const uint32_t*>(&v1));
+    for (int c = 0; c < 2; ++c) {
+        uint4 pk;
+        pk.x = pack_bf16x2(acc[8 * c] * inv, acc[8 * c + 1] * inv);
+        pk.y = pack_bf16x2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
+        pk.z = pack_bf16x2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
+        pk.w = pack_bf16x2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
+        o[c] = pk;
     }
-    if (lse && part == 0) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+    if (lse && (threadIdx.x & 31) == 0) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 // CTAs per query row.  One CTA fills an SM's shared memory, so the grid
@@ -579,8 +584,8 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
     if (e != cudaSuccess) return e;
     count_launches(1);
     if (splits == 1) return e;
-    merge_kernel<<<dim3(rows_per_seq, bd.B), 256, 0, stream>>>(bd, rr, rows_per_seq, splits, part_o, part_lse,
-                                                              out, lse, status);
+    merge_kernel<<<dim3(rows_per_seq * 8, bd.B), 256, 0, stream>>>(bd, rr, rows_per_seq, splits, part_o,
+                                                                  part_lse, out, lse, status);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;

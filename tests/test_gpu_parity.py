@@ -196,3 +196,26 @@ def test_empty_batch_is_noop():
     f = torch.empty(16, dtype=torch.float32, device="cuda")
     dsa.forward(b, z, f, z, z, z, 4, 0.0625, z, ws=ws)
     assert dsa.read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("T,rows", [(33000, 3), (340000, 2)])
+def test_topk_cluster_slices_and_global_fallback(T, rows):
+    # T = 33000: a cluster of 5 CTAs, each slice in shared memory; the tied
+    # rows make the k-th value straddle slice boundaries.  T = 340000: a
+    # cluster of 8 whose slices exceed shared memory (global-memory path).
+    rng = np.random.default_rng(T)
+    k = 2048
+    bt = W.Batch(B=1, stride=T, q_off=np.array([0, rows], np.int32), ctx_len=np.array([T], np.int32),
+                 q_idx=None, w=None, k_idx=None, q=None, kv=None, k=k, sm_scale=W.SM_SCALE)
+    s = rng.standard_normal((rows, T)).astype(np.float32)
+    s[0, :] = 0.5                                   # all tied: the first k positions win
+    s[1, ::3] = 7.0                                 # ties far above the rest, across every slice
+    b = dsa.make_batch(bt.q_off, bt.ctx_len, rows, T, T)
+    sc = torch.from_numpy(s).cuda()
+    ix = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    ws = dsa.workspace(b, k)
+    dsa.topk(b, sc, k, ix, ws=ws)
+    assert dsa.read_device_status(ws) == 0
+    got = ix.cpu().numpy()
+    assert np.array_equal(got, oracle.topk(bt, s, k=k))
+    assert np.array_equal(got[0], np.arange(k))
