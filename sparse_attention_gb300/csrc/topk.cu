@@ -5,29 +5,36 @@
 // selection must be deterministic; the GLM-5 explainer page: a query that
 // sees fewer than 2048 positions keeps all of them.)
 //
-// One CTA per query row.  Scores map to order-preserving 32-bit keys (-0.0
-// folded onto +0.0).  The selection is:
-//   1. a lower bound L for the k-th largest key: the lower edge of the
+// One thread-block cluster of C CTAs per query row (C = 1 unless rows are
+// long and few); CTA r owns the r-th contiguous slice of the row.  Scores
+// map to order-preserving 32-bit keys (-0.0 folded onto +0.0).
+//   1. A lower bound L for the k-th largest key: the lower edge of the
 //      leading-digit bin (top 11 bits) holding the (r+1)-th largest of 1024
-//      evenly spaced keys, r sized so that well over k keys of the row lie
-//      at or above it;
-//   2. one pass over the row (16-byte loads): warp w owns a contiguous
-//      segment and appends its keys >= L, in position order, to a region of
-//      shared memory of its own (warp scans give the slots);
-//   3. the exact k-th largest key tau among these candidates by a radix
-//      select over three digits (11 + 11 + 10 bits), shared-memory
-//      histograms restricted to the keys matching the digits found so far;
-//   4. the output, warp by warp in position order: candidates above tau,
-//      and the first `need` candidates equal to tau (ties go to the lower
-//      position), each written at its rank; positions come out ascending.
+//      evenly spaced keys of the whole row, r sized so that well over k keys
+//      lie at or above it.  Every CTA of the cluster derives the same L.
+//   2. One pass over the slice (16-byte loads, several in flight): warp w of
+//      a CTA owns a contiguous segment and appends its keys >= L, in
+//      position order, to a shared-memory region of its own.
+//   3. The exact k-th largest key tau among the candidates of the cluster:
+//      a radix select over three digits (11 + 11 + 10 bits); each CTA counts
+//      its candidates and every CTA sums the cluster's histograms through
+//      distributed shared memory, so all derive the same digits.
+//   4. The output in position order: candidates above tau and the first
+//      `need` candidates equal to tau (ties go to the lower position), each
+//      written at its rank; ranks add the counts of lower warps and lower
+//      CTAs.  Positions come out ascending.
 // Every key that is not a candidate lies below L <= tau, so the result is
-// exactly the top-k of the row.  When the sample misjudges (fewer than k
-// candidates, or a warp's region overflows) the same select and an ordered
-// output run over the whole row.  Atomics only count, so the result is the
-// same bit for bit on every run.
+// exactly the top-k of the row.  If the sample misjudges (fewer than k
+// candidates in the cluster, or a full region) steps 3-4 run over the whole
+// slices instead.  Atomics only count; the result is the same bit for bit
+// on every run.
+#include <cooperative_groups.h>
+
 #include <algorithm>
 
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 namespace {
@@ -38,8 +45,11 @@ constexpr int kBins = 2048;
 constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kSample = 1024;
 constexpr int kRegion = 512;                 // candidate slots per warp
-constexpr int kMaxCand = kWarps * kRegion;   // 8192
+constexpr int kMaxCand = kWarps * kRegion;   // 8192 per CTA
 constexpr int kPrefetch = 6;                 // 16-byte loads in flight per lane
+constexpr int kMaxCluster = 8;
+constexpr int kLongRow = 65536;              // rows above this may be split over a cluster
+constexpr int kKeysPerCta = 32768;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
@@ -64,17 +74,18 @@ struct alignas(16) TopkSmem {
     int32_t cand_pos[kMaxCand];
     uint32_t warp_sums[32];
     uint32_t wcnt[32], wgt[32], weq[32];
-    uint32_t total, sel_digit, sel_above, ok, chunk_total;
+    uint32_t total, sel_digit, sel_above, chunk_total;
+    uint32_t cta_cand, cta_overflow, cta_gt, cta_eq;   // read by the rest of the cluster
 };
 
-// The k-th largest of the keys j in [0, m) with valid_of(j), resolved to the
-// first `passes` digits (3 = exact): returns tau (the digits found, zero
-// below them) and sets need = how many keys matching tau belong to the top
-// k.  S.hist must be zero on entry and is zero on return.  Four barriers
-// per digit.
+// The k-th largest of the keys j in [0, m) with valid_of(j), over this CTA
+// (nranks == 1) or over the whole cluster (nranks == cluster size), resolved
+// to the first `passes` digits (3 = exact): returns tau (the digits found,
+// zero below) and sets need = how many keys matching tau belong to the top
+// k.  S.hist must be zero on entry; zero on return.
 template <typename KeyOf, typename ValidOf>
-__device__ uint32_t radix_select(TopkSmem& S, int32_t m, uint32_t k, int passes, KeyOf key_of, ValidOf valid_of,
-                                 uint32_t& need_out) {
+__device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSmem& S, int32_t m, uint32_t k,
+                                 int passes, KeyOf key_of, ValidOf valid_of, uint32_t& need_out) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0u, pmask = 0u, need = k;
 #pragma unroll 1
@@ -86,17 +97,30 @@ __device__ uint32_t radix_select(TopkSmem& S, int32_t m, uint32_t k, int passes,
             const uint32_t key = key_of(j);
             if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> sh) & dmask], 1u);
         }
-        __syncthreads();
-        // thread tid owns bins [4 tid, 4 tid + 4) (read, then cleared for
-        // the next digit); keys in higher bins = total - inclusive scan
+        // thread tid owns bins [4 tid, 4 tid + 4), summed over the ranks
         uint32_t c[kBinsPerThread];
         uint32_t mine = 0u;
+        if (nranks == 1) {
+            __syncthreads();
+#pragma unroll
+            for (int x = 0; x < kBinsPerThread; ++x) c[x] = S.hist[kBinsPerThread * tid + x];
+        } else {
+            cluster.sync();
+#pragma unroll
+            for (int x = 0; x < kBinsPerThread; ++x) c[x] = 0u;
+            for (int r = 0; r < nranks; ++r) {
+                const uint32_t* h = cluster.map_shared_rank(S.hist, r);
+#pragma unroll
+                for (int x = 0; x < kBinsPerThread; ++x) c[x] += h[kBinsPerThread * tid + x];
+            }
+            cluster.sync();                        // every remote read done before any bin is cleared
+        }
 #pragma unroll
         for (int x = 0; x < kBinsPerThread; ++x) {
-            c[x] = S.hist[kBinsPerThread * tid + x];
             S.hist[kBinsPerThread * tid + x] = 0u;
             mine += c[x];
         }
+        // keys in higher bins = total - inclusive scan in bin order
         const uint32_t incl_w = warp_inclusive_scan(mine);
         if (lane == 31) S.warp_sums[warp] = incl_w;
         __syncthreads();
@@ -107,7 +131,7 @@ __device__ uint32_t radix_select(TopkSmem& S, int32_t m, uint32_t k, int passes,
             if (lane == kWarps - 1) S.total = sc;
         }
         __syncthreads();
-        uint32_t above = S.total - (incl_w + (warp ? S.warp_sums[warp - 1] : 0u));   // bins above this thread's
+        uint32_t above = S.total - (incl_w + (warp ? S.warp_sums[warp - 1] : 0u));
 #pragma unroll
         for (int x = kBinsPerThread - 1; x >= 0; --x) {
             if (above < need && need <= above + c[x]) {
@@ -125,17 +149,34 @@ __device__ uint32_t radix_select(TopkSmem& S, int32_t m, uint32_t k, int passes,
     return prefix;
 }
 
+// Exclusive prefix over the cluster's lower ranks of the CTA counts (gt, eq)
+// stored in S.cta_gt / S.cta_eq; call after a cluster barrier.
+__device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, int crank, TopkSmem& S, uint32_t& gt0,
+                                               uint32_t& eq0) {
+    gt0 = 0u;
+    eq0 = 0u;
+    for (int r = 0; r < crank; ++r) {
+        const TopkSmem* o = cluster.map_shared_rank(&S, r);
+        gt0 += o->cta_gt;
+        eq0 += o->cta_eq;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
     topk_kernel(const BatchDev bd, const RowRange rr, const float* __restrict__ scores, const int64_t ld,
                 const int scores_local, const int k, int32_t* __restrict__ idx, const int idx_local,
-                int32_t* status) {
+                const int csize, int32_t* status) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     TopkSmem& S = *reinterpret_cast<TopkSmem*>(smem_raw);
+    cg::cluster_group cluster = cg::this_cluster();
 
+    // every test below depends only on the row, so all CTAs of a cluster
+    // take the same branch and reach the same cluster barriers
     const int b = blockIdx.y;
     SeqInfo sq;
     if (!load_seq(bd, b, status, sq)) return;
-    const int32_t i = rr.i0 + (int32_t)blockIdx.x;
+    const int crank = (int)(blockIdx.x % (unsigned)csize);
+    const int32_t i = rr.i0 + (int32_t)(blockIdx.x / (unsigned)csize);
     if (i >= min(rr.i1, sq.nq)) return;
     const int32_t t = sq.ctx - sq.nq + i;
     const int32_t n = t + 1;
@@ -144,13 +185,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (n <= k) {  // every causal position is selected
-        for (int j = tid; j < k; j += kThreads) out[j] = j < n ? j : -1;
+        if (crank == 0)
+            for (int j = tid; j < k; j += kThreads) out[j] = j < n ? j : -1;
         return;
     }
     auto row_key = [&](int32_t j) -> uint32_t { return order_key(__ldg(row + j)); };
 
-    // 1. the lower bound L: the smallest key of the leading-digit bin that
-    //    holds the (r+1)-th largest sampled key
+    // this CTA's slice [s_lo, s_hi) of the row (slices start on multiples of 128)
+    const int32_t span = ((n + csize - 1) / csize + 127) & ~127;
+    const int32_t s_lo = min(n, crank * span), s_hi = min(n, s_lo + span);
+
+    // 1. the lower bound L (the same in every CTA)
     const int32_t ns = min(n, kSample);
 #pragma unroll
     for (int x = 0; x < kBinsPerThread; ++x) S.hist[kBinsPerThread * tid + x] = 0u;
@@ -159,12 +204,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float expect = (float)k * (float)ns / (float)n;
     const int32_t r = min(ns - 1, (int32_t)(1.25f * expect + 3.f * sqrtf(expect)) + 8);
     uint32_t unused;
-    const uint32_t L = radix_select(
-        S, ns, (uint32_t)(r + 1), 1, [&](int32_t j) { return S.sample[j]; }, [](int32_t) { return true; }, unused);
+    const uint32_t L = radix_select(cluster, 1, S, ns, (uint32_t)(r + 1), 1, [&](int32_t j) { return S.sample[j]; },
+                                    [](int32_t) { return true; }, unused);
 
     // 2. one pass: warp w appends its keys >= L to its region, in order
-    const int32_t seg = ((n + kWarps - 1) / kWarps + 127) & ~127;
-    const int32_t w_lo = min(n, warp * seg), w_hi = min(n, w_lo + seg);
+    const int32_t seg = ((s_hi - s_lo + kWarps - 1) / kWarps + 127) & ~127;
+    const int32_t w_lo = min(s_hi, s_lo + warp * seg), w_hi = min(s_hi, w_lo + seg);
     uint32_t* rk = S.cand_key + warp * kRegion;
     int32_t* rp = S.cand_pos + warp * kRegion;
     uint32_t cnt = 0u;
@@ -203,17 +248,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t c = lane < kWarps ? S.wcnt[lane] : 0u;
         const uint32_t tot = warp_inclusive_scan(c);
         const bool overflow = __any_sync(0xffffffffu, c > (uint32_t)kRegion);
-        if (lane == 31) S.ok = (!overflow && tot >= (uint32_t)k) ? 1u : 0u;
+        if (lane == 31) {
+            S.cta_cand = tot;
+            S.cta_overflow = overflow ? 1u : 0u;
+        }
     }
-    __syncthreads();
+    cluster.sync();
+    uint32_t all_cand = 0u, any_overflow = 0u;
+    for (int q = 0; q < csize; ++q) {
+        const TopkSmem* o = cluster.map_shared_rank(&S, q);
+        all_cand += o->cta_cand;
+        any_overflow |= o->cta_overflow;
+    }
+    const bool use_candidates = !any_overflow && all_cand >= (uint32_t)k;
 
     uint32_t need;
-    if (S.ok) {
-        // 3. tau among the candidates (slots past a region's count are empty)
+    if (use_candidates) {
+        // 3. tau among the cluster's candidates (slots past a count are empty)
         const uint32_t tau = radix_select(
-            S, kMaxCand, (uint32_t)k, 3, [&](int32_t j) { return S.cand_key[j]; },
+            cluster, csize, S, kMaxCand, (uint32_t)k, 3, [&](int32_t j) { return S.cand_key[j]; },
             [&](int32_t j) { return (uint32_t)(j % kRegion) < S.wcnt[j / kRegion]; }, need);
-        // 4. ordered output: counts per warp region, prefix over warps, write
+        // 4. ordered output: counts per warp, prefix over warps and lower CTAs
         const uint32_t c = S.wcnt[warp];
         uint32_t g = 0u, e = 0u;
         for (uint32_t s0 = 0; s0 < c; s0 += 32) {
@@ -235,9 +290,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                 S.wgt[lane] = gi - gv;
                 S.weq[lane] = ei - ev;
             }
+            if (lane == 31) {
+                S.cta_gt = gi;
+                S.cta_eq = ei;
+            }
         }
-        __syncthreads();
-        uint32_t gt_run = S.wgt[warp], eq_run = S.weq[warp];
+        cluster.sync();
+        uint32_t gt0, eq0;
+        cluster_prefix(cluster, crank, S, gt0, eq0);
+        uint32_t gt_run = gt0 + S.wgt[warp], eq_run = eq0 + S.weq[warp];
         const uint32_t lower = (1u << lane) - 1u;
         for (uint32_t s0 = 0; s0 < c; s0 += 32) {
             const uint32_t s = s0 + lane;
@@ -251,24 +312,49 @@ __global__ void __launch_bounds__(kThreads, 2)
             eq_run += __popc(be);
         }
     } else {
-        // the sample misjudged: select and write over the whole row
-        const uint32_t tau = radix_select(S, n, (uint32_t)k, 3, row_key, [](int32_t) { return true; }, need);
-        uint32_t gt_run = 0u, eq_run = 0u;
+        // the sample misjudged: select and write over the whole slices
+        const int32_t len = s_hi - s_lo;
+        auto slice_key = [&](int32_t j) -> uint32_t { return row_key(s_lo + j); };
+        const uint32_t tau =
+            radix_select(cluster, csize, S, len, (uint32_t)k, 3, slice_key, [](int32_t) { return true; }, need);
+        uint32_t g = 0u, e = 0u;
+        for (int32_t j = tid; j < len; j += kThreads) {
+            const uint32_t key = slice_key(j);
+            g += key > tau;
+            e += key == tau;
+        }
+        const uint32_t gw = warp_inclusive_scan(g), ew = warp_inclusive_scan(e);
+        if (lane == 31) {
+            S.wgt[warp] = gw;
+            S.weq[warp] = ew;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const uint32_t gs = warp_inclusive_scan(lane < kWarps ? S.wgt[lane] : 0u);
+            const uint32_t es = warp_inclusive_scan(lane < kWarps ? S.weq[lane] : 0u);
+            if (lane == 31) {
+                S.cta_gt = gs;
+                S.cta_eq = es;
+            }
+        }
+        cluster.sync();
+        uint32_t gt_run, eq_run;
+        cluster_prefix(cluster, crank, S, gt_run, eq_run);
         constexpr int kE = 4;
 #pragma unroll 1
-        for (int32_t base = 0; base < n; base += kThreads * kE) {
+        for (int32_t base = 0; base < len; base += kThreads * kE) {
             const int32_t j0 = base + tid * kE;
             uint32_t kk[kE];
-            uint32_t g = 0u, e = 0u;
+            uint32_t gc = 0u, ec = 0u;
 #pragma unroll
             for (int x = 0; x < kE; ++x) {
-                kk[x] = j0 + x < n ? row_key(j0 + x) : 0u;
-                if (j0 + x < n) {
-                    g += kk[x] > tau;
-                    e += kk[x] == tau;
+                kk[x] = j0 + x < len ? slice_key(j0 + x) : 0u;
+                if (j0 + x < len) {
+                    gc += kk[x] > tau;
+                    ec += kk[x] == tau;
                 }
             }
-            const uint32_t wi = warp_inclusive_scan(g | (e << 16));
+            const uint32_t wi = warp_inclusive_scan(gc | (ec << 16));
             if (lane == 31) S.warp_sums[warp] = wi;
             __syncthreads();
             if (warp == 0) {
@@ -278,16 +364,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             __syncthreads();
             const uint32_t packed = wi + (warp ? S.warp_sums[warp - 1] : 0u);
-            uint32_t gtb = gt_run + (packed & 0xFFFFu) - g;
-            uint32_t eqb = eq_run + (packed >> 16) - e;
+            uint32_t gtb = gt_run + (packed & 0xFFFFu) - gc;
+            uint32_t eqb = eq_run + (packed >> 16) - ec;
 #pragma unroll
             for (int x = 0; x < kE; ++x) {
-                if (j0 + x < n) {
+                if (j0 + x < len) {
                     if (kk[x] > tau) {
-                        out[gtb + min(eqb, need)] = j0 + x;
+                        out[gtb + min(eqb, need)] = s_lo + j0 + x;
                         ++gtb;
                     } else if (kk[x] == tau) {
-                        if (eqb < need) out[gtb + eqb] = j0 + x;
+                        if (eqb < need) out[gtb + eqb] = s_lo + j0 + x;
                         ++eqb;
                     }
                 }
@@ -297,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncthreads();
         }
     }
+    cluster.sync();                                // the cluster may still read this CTA's counts
 }
 
 }  // namespace
@@ -305,13 +392,28 @@ cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, in
                         int k, int32_t* idx, bool idx_local, int32_t* status, cudaStream_t stream) {
     const int32_t rows_per_seq = min(rr.i1, bd.max_q) - rr.i0;
     if (rows_per_seq <= 0) return cudaSuccess;
+    // long rows, few of them: split each row over a cluster
+    const int64_t rows = (int64_t)rows_per_seq * bd.B;
+    int csize = 1;
+    if (bd.max_ctx > kLongRow && rows < 2 * kNumSMs)
+        csize = (int)std::min<int64_t>(kMaxCluster, ((int64_t)bd.max_ctx + kKeysPerCta - 1) / kKeysPerCta);
     const size_t smem = sizeof(TopkSmem);
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)rows_per_seq, (unsigned)bd.B);
-    topk_kernel<<<grid, kThreads, smem, stream>>>(bd, rr, scores, ld, scores_local ? 1 : 0, k, idx,
-                                                  idx_local ? 1 : 0, status);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows_per_seq * csize), (unsigned)bd.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, topk_kernel, bd, rr, scores, ld, scores_local ? 1 : 0, k, idx, idx_local ? 1 : 0,
+                           csize, status);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }

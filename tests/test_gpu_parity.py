@@ -198,11 +198,12 @@ def test_empty_batch_is_noop():
     assert dsa.read_device_status(ws) == 0
 
 
-@pytest.mark.parametrize("T,rows", [(33000, 3), (340000, 2)])
+@pytest.mark.parametrize("T,rows", [(33000, 3), (100000, 3), (340000, 2)])
 def test_topk_cluster_slices_and_global_fallback(T, rows):
-    # T = 33000: a cluster of 5 CTAs, each slice in shared memory; the tied
-    # rows make the k-th value straddle slice boundaries.  T = 340000: a
-    # cluster of 8 whose slices exceed shared memory (global-memory path).
+    # Rows 0 and 1 are tied so heavily that the sampled bound keeps too many
+    # candidates (the whole-row select runs); row 2 is random (the candidate
+    # select runs).  T = 100000 and 340000 split each row over a cluster of
+    # 4 and 8 CTAs, so tied runs straddle the slices of different CTAs.
     rng = np.random.default_rng(T)
     k = 2048
     bt = W.Batch(B=1, stride=T, q_off=np.array([0, rows], np.int32), ctx_len=np.array([T], np.int32),
