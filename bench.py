@@ -376,6 +376,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- multi-rank --
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_step_per_rank: float, steps: int, world: int, ms_max: float) -> float:
+    """Units processed by all ranks per second of the slowest rank's time
+    (weak scaling: every rank runs its own batch)."""
+    return units_per_step_per_rank * steps * world / (ms_max / 1e3)
+
+
 # --------------------------------------------------------------------- dsa --
 
 def traffic_from_profiles(kernel: str, workload: str):
@@ -427,13 +446,6 @@ def run_dsa(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     clocks = ClockSampler(local)
     clocks.start()
     for i in range(Wu):
@@ -450,15 +462,14 @@ def run_dsa(args):
     barrier()
     clocks.timed(t_start, time.time())
     launches = dsa.kernel_launch_count() - n0
-    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
     status = dsa.read_device_status(case.ws[0])
-    units = case.units_per_step * K * world
-    value = units / (ms / 1e3)
+    value = whole_job_value(case.units_per_step, K, world, ms)
 
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(case, K, Wu, barrier, max_over_ranks, world)
+        e2e = run_e2e(case, K, Wu, barrier, lambda x: max_over_ranks(x, dev), world)
 
     # per-kernel device times and the roofline of the dominant kernel
     times = case.kernel_times_us(args.kernel_reps)
@@ -548,7 +559,7 @@ def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
     e1.record(stream)
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1))
-    value = case.units_per_step * K * world / (ms / 1e3)
+    value = whole_job_value(case.units_per_step, K, world, ms)
     return {"value": value, "unit": case.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "sparse_attention_gb300.forward"}
 

@@ -119,6 +119,14 @@ DSA_API const char* dsa_last_cuda_error(void);
  * devices, all streams).  Instrumentation for benchmarks; host only. */
 DSA_API uint64_t dsa_kernel_launch_count(void);
 
+/* Diagnostic for the failure path: launches one CTA whose thread waits on a
+ * barrier phase that nothing completes, bounded by limit_us (1 .. 10^6
+ * microseconds).  The wait gives up, latches DSA_ERR_TIMEOUT in the status
+ * word of ws (as every kernel of the path does when one of its bounded waits
+ * expires) and the kernel returns normally: no trap, no hang, the context
+ * stays usable.  Read the result with dsa_read_device_status. */
+DSA_API dsa_status dsa_selftest_wait_timeout(void* ws, uint32_t limit_us, void* stream);
+
 /* Step 1: lightning-indexer scores.
  *   q_idx  bf16 [total_q, 32, 128]  post-RoPE index queries
  *   w      fp32 [total_q, 32]       head weights

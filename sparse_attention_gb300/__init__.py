@@ -31,7 +31,8 @@ STATUS = {
 }
 
 EXPORTS = ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
-           "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd", "dsa_sparse_mla_fwd_noalloc", "dsa_forward")
+           "dsa_selftest_wait_timeout", "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd",
+           "dsa_sparse_mla_fwd_noalloc", "dsa_forward")
 
 
 class DsaError(RuntimeError):
@@ -76,6 +77,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_topk.argtypes = [BP, P, i64, i32, P, P, sz, P]
     lib.dsa_sparse_mla_fwd.argtypes = [BP, P, P, P, i32, f32, P, P, P, sz, P]
     lib.dsa_sparse_mla_fwd_noalloc.argtypes = [BP, P, P, P, i32, f32, P, P, P, P]
+    lib.dsa_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
     lib.dsa_forward.argtypes = [BP, P, P, P, P, P, i32, f32, P, P, P, P, i64, P, sz, P]
     for name in EXPORTS:
         if name not in ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count"):
@@ -175,6 +177,12 @@ def read_device_status(ws: torch.Tensor, stream=None) -> int:
     v = ctypes.c_int(0)
     _check(load_library().dsa_read_device_status(_p(ws), _stream(stream), ctypes.byref(v)), "dsa_read_device_status")
     return int(v.value)
+
+
+def selftest_wait_timeout(ws: torch.Tensor, limit_us: int = 2000, stream=None) -> None:
+    """Launch the bounded-wait diagnostic (see dsa_selftest_wait_timeout)."""
+    _check(load_library().dsa_selftest_wait_timeout(_p(ws), int(limit_us), _stream(stream)),
+           "dsa_selftest_wait_timeout")
 
 
 def indexer_scores(batch: Batch, q_idx, w, k_idx, scores, ld: Optional[int] = None, ws=None, stream=None):
