@@ -62,7 +62,7 @@ def parse_args():
 
 
 def default_steps(wl: W.Workload):
-    return (300, 10) if wl.kind == "decode" else (20, 3)
+    return (300, 10) if wl.kind in ("decode", "indexshare") else (20, 3)
 
 
 def load_peaks():
@@ -77,6 +77,9 @@ def load_peaks():
 # --------------------------------------------------------------- workloads --
 
 def metric_for(wl: W.Workload):
+    if wl.kind == "indexshare":
+        return (f"IndexShare decode window steps/s ({wl.B} seqs x {wl.ctx} ctx, 1 full + {wl.steps - 1} shared "
+                f"layers, top-{wl.k})", "steps/s")
     if wl.kind == "decode":
         return f"decode steps/s ({wl.B} seqs x {wl.ctx} ctx, top-{wl.k}; % of HBM roofline)", "steps/s"
     if wl.kind == "prefill":
@@ -86,7 +89,7 @@ def metric_for(wl: W.Workload):
 
 def base_config(wl: W.Workload, world: int):
     return {"workload": wl.name, "batch": wl.B, "ctx": wl.ctx, "queries_per_seq": wl.n_new, "topk": wl.k,
-            "l2": "no flush: inputs larger than L2" if wl.kind == "decode" else
+            "l2": "no flush: inputs larger than L2" if wl.kind in ("decode", "indexshare") else
             "no flush: the one sequence's keys and latent cache are L2-resident by design",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -110,6 +113,21 @@ class Case:
             self.batches = [dsa.Batch(bt.q_off, c, 1, wl.ctx, bt.stride, total_q=wl.B) for c in self.ctx_variants]
             self.positions = [[wl.ctx - wl.steps + j] * wl.B for j in range(wl.steps)]
             self.units_per_step = 1            # one decode step of the whole batch
+        elif wl.kind == "indexshare":
+            # layer 0 is full; layers 1.. reuse its indices with their own q and latent cache
+            self.bt = W.make_batch_torch([wl.ctx] * wl.B, [1] * wl.B, wl.k, seed, key_kind=wl.key_kind,
+                                         device=device, name=wl.name)
+            bt = self.bt
+            self.shared = []
+            for layer in range(1, wl.steps):
+                lb = W.make_batch_torch([wl.ctx] * wl.B, [1] * wl.B, wl.k, seed + 17 * layer, key_kind="iid",
+                                        device=device)
+                self.shared.append((lb.q, lb.kv))
+                del lb
+            self.batches = [dsa.Batch(bt.q_off, bt.ctx_len, 1, wl.ctx, bt.stride, total_q=wl.B)]
+            self.positions = [[wl.ctx - 1] * wl.B]
+            self.units_per_step = 1            # one decode step of the whole window
+            self.share_idx = torch.empty((wl.B, wl.k), dtype=torch.int32, device=device)
         elif wl.kind == "prefill":
             self.bt = W.make_batch_torch([wl.ctx], [wl.n_new], wl.k, seed, key_kind=wl.key_kind, device=device,
                                          name=wl.name)
@@ -147,6 +165,14 @@ class Case:
     def step(self, i=0):
         """One step of the workload: every dsa_forward call it needs."""
         wl = self.wl
+        if wl.kind == "indexshare":
+            b = self.batches[0]
+            self.dsa.forward(b, self.bt.q_idx, self.bt.w, self.bt.k_idx, self.bt.q, self.bt.kv, wl.k,
+                             self.bt.sm_scale, self.out, self.lse, idx_out=self.share_idx, ws=self.ws[0])
+            for q, kv in self.shared:
+                self.dsa.sparse_mla_fwd(b, q, kv, self.share_idx, wl.k, self.bt.sm_scale, self.out, self.lse,
+                                        ws=self.ws[0])
+            return
         if wl.kind == "decode":
             j = i % len(self.batches)
             calls = [j]
@@ -161,7 +187,7 @@ class Case:
     # algorithmic work of one step
     def work(self):
         wl = self.wl
-        calls = [0] if wl.kind == "decode" else range(len(self.batches))
+        calls = [0] if wl.kind in ("decode", "indexshare") else range(len(self.batches))
         idx_flop = idx_bytes = att_flop = att_bytes = topk_bytes = 0
         for j in calls:
             pos = self.positions[j]
@@ -171,7 +197,10 @@ class Case:
             att_flop += ATT_FLOP_PER_SEL * sel
             att_bytes += ATT_BYTES_PER_SEL * sel + ATT_BYTES_PER_QUERY * len(pos)
             topk_bytes += 4 * pairs + 4 * wl.k * len(pos)
-            if wl.kind == "decode":
+            if wl.kind == "indexshare":   # the shared layers repeat the attention only
+                att_flop *= wl.steps
+                att_bytes *= wl.steps
+            if wl.kind in ("decode", "indexshare"):
                 idx_bytes += IDX_BYTES_PER_KEY * sum(t + 1 for t in pos) + IDX_BYTES_PER_QUERY * len(pos)
             else:   # one sequence: keys read once per call (they stay in L2 across query groups)
                 idx_bytes += IDX_BYTES_PER_KEY * (max(pos) + 1) + IDX_BYTES_PER_QUERY * len(pos)
@@ -216,7 +245,7 @@ class Case:
         pos = self.positions[0]
         pairs = sum(t + 1 for t in pos)
         sel = sum(min(wl.k, t + 1) for t in pos)
-        if wl.kind == "decode":
+        if wl.kind in ("decode", "indexshare"):
             ib = IDX_BYTES_PER_KEY * pairs + IDX_BYTES_PER_QUERY * len(pos)
         else:
             ib = IDX_BYTES_PER_KEY * (max(pos) + 1) + IDX_BYTES_PER_QUERY * len(pos)
@@ -310,12 +339,15 @@ def host_sample(case: Case, n_seq: int):
     return b, rows, len(rows), f"{len(rows)} evenly spaced query rows of the {T}-token prefill"
 
 
-def oracle_path_seconds(b, rows):
+def oracle_path_seconds(b, rows, attention_layers: int = 1):
+    """The oracle's whole path on `rows`; attention_layers > 1 repeats the
+    attention on the same indices (IndexShare's shared layers)."""
     import oracle
     t0 = time.perf_counter()
     sc = oracle.indexer_scores(b, rows)
     ix = oracle.topk(b, np.nan_to_num(sc.astype(np.float32), nan=0.0), rows=rows, k=b.k)
-    oracle.sparse_mla(b, ix, rows=rows)
+    for _ in range(attention_layers):
+        oracle.sparse_mla(b, ix, rows=rows)
     return time.perf_counter() - t0
 
 
@@ -342,7 +374,8 @@ def run_reference(args):
     K = args.steps if args.steps is not None else K
     Wu = args.warmup if args.warmup is not None else Wu
     # one bounded sample per step, drawn with the numpy recipe
-    if wl.kind == "decode":
+    shared_layers = wl.steps - 1 if wl.kind == "indexshare" else 0
+    if wl.kind in ("decode", "indexshare"):
         ns = 1
         b = W.make_batch_np([wl.ctx] * ns, [1] * ns, wl.k, wl.seed, key_kind=wl.key_kind)
         rows = list(range(ns))
@@ -358,11 +391,14 @@ def run_reference(args):
         rows = [int(x) for x in np.linspace(0, T - 1, nq)]
         frac = nq
         sample = f"{nq} evenly spaced query rows per timed step"
+    def one_step():
+        oracle_path_seconds(b, rows, 1 + shared_layers)
+
     for _ in range(Wu):
-        oracle_path_seconds(b, rows)
+        one_step()
     t0 = time.perf_counter()
     for _ in range(K):
-        oracle_path_seconds(b, rows)
+        one_step()
     secs = (time.perf_counter() - t0) / K
     value = frac / secs
     metric, unit = metric_for(wl)
@@ -468,7 +504,7 @@ def run_dsa(args):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and wl.kind != "indexshare":
         e2e = run_e2e(case, K, Wu, barrier, lambda x: max_over_ranks(x, dev), world)
 
     # per-kernel device times and the roofline of the dominant kernel
@@ -478,7 +514,7 @@ def run_dsa(args):
     peaks, peak_src = load_peaks()
     dom = max(times, key=times.get)
     kw = work[dom]
-    if wl.kind != "decode" and dom in ("indexer", "sparse_mla"):
+    if wl.kind not in ("decode", "indexshare") and dom in ("indexer", "sparse_mla"):
         achieved = kw["flop"] / (times[dom] * 1e-6) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"]}
@@ -494,7 +530,7 @@ def run_dsa(args):
     if rank != 0:
         return
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and wl.kind != "indexshare":
         cpu = cpu_baseline(case, case.unit)
     wk = case.work()
     cfg = base_config(wl, world)
@@ -502,7 +538,7 @@ def run_dsa(args):
                                         "attention_tflop": wk["att_flop"] / 1e12,
                                         "indexer_gb": wk["idx_bytes"] / 1e9, "attention_gb": wk["att_bytes"] / 1e9},
                "device_status": status}
-    if wl.kind == "decode":
+    if wl.kind in ("decode", "indexshare"):
         details["tokens_per_s"] = value * wl.B
     line = {"metric": case.metric, "value": value, "unit": case.unit, "n_gpus": world, "steps": K, "warmup": Wu,
             "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

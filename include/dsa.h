@@ -155,7 +155,11 @@ DSA_API dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t
  *   out bf16 [total_q, 64, 512]            softmax(sm_scale * q.kv) @ kv[:, :512]
  *   lse fp32 [total_q, 64] or NULL         natural-log sum-exp of the logits
  * A row with no valid index gets out = 0 and lse = -inf.  Entries outside
- * [-1, t] latch DSA_ERR_BAD_INDEX and are skipped. */
+ * [-1, t] latch DSA_ERR_BAD_INDEX and are skipped.
+ * IndexShare ("GLM-5.2 架构 QA", Q2.1-Q2.2): a "shared" layer skips the
+ * indexer and the top-k and reuses the indices of the last "full" layer;
+ * it is this call with that layer's idx (dsa_forward's idx_out) and the
+ * shared layer's own q and latent cache. */
 DSA_API dsa_status dsa_sparse_mla_fwd(const dsa_batch* batch, const uint16_t* q, const uint16_t* kv,
                               const int32_t* idx, int k, float sm_scale, uint16_t* out, float* lse,
                               void* ws, size_t ws_bytes, void* stream);

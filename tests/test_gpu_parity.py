@@ -220,3 +220,18 @@ def test_topk_cluster_slices_and_global_fallback(T, rows):
     got = ix.cpu().numpy()
     assert np.array_equal(got, oracle.topk(bt, s, k=k))
     assert np.array_equal(got[0], np.arange(k))
+
+
+def test_indexshare_window_reuses_the_full_layers_indices():
+    # IndexShare: layer 0 runs the whole path; layers 1 and 2 ("shared") run
+    # attention only, on their own q and latent cache, with layer 0's indices
+    full = W.make_batch_np([3000, 2500, 700], [1, 1, 1], k=512, seed=81, key_kind="zipf")
+    st = Staged(full)
+    out0, lse0, idx, _ = st.forward()
+    check_attention(st, idx, out0, lse0)
+    for layer in (1, 2):
+        lb = W.make_batch_np([3000, 2500, 700], [1, 1, 1], k=512, seed=81 + 10 * layer)
+        sl = Staged(lb)
+        out, lse = sl.attention(idx)
+        check_attention(sl, idx, out, lse)          # the shared layer against the oracle on the reused indices
+        assert sl.status() == 0

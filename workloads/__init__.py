@@ -231,6 +231,10 @@ WORKLOADS: Dict[str, Workload] = {
     # chunked prefill: 65536 tokens in 8 chunks of 8192 queries
     "chunked_prefill_T65536_c8192": Workload("chunked_prefill_T65536_c8192", "chunked_prefill", 1, 65536, 8192,
                                              TOPK, "lowrank16", 20263, steps=8),
+    # IndexShare window on the decode shape: one full layer (indexer, top-k,
+    # attention) and three shared layers reusing its indices (steps = layers)
+    "indexshare_decode_B64_ctx32768_w4": Workload("indexshare_decode_B64_ctx32768_w4", "indexshare", 64, 32768, 1,
+                                                  TOPK, "iid", 20265, steps=4),
     # long decode: 8 sequences at 202752 context, 4 decode steps
     "long_decode_B8_ctx202752": Workload("long_decode_B8_ctx202752", "decode", 8, MAX_POS, 1, TOPK, "zipf",
                                          20264, steps=4),
