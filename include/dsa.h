@@ -78,7 +78,8 @@ typedef enum dsa_status {
     DSA_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
     DSA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel expired */
     DSA_ERR_BAD_BATCH = 6,   /* device: q_off / ctx_len outside the host bounds */
-    DSA_ERR_BAD_INDEX = 7    /* device: a selected index outside [-1, t] */
+    DSA_ERR_BAD_INDEX = 7,   /* device: a selected index outside [-1, t] */
+    DSA_ERR_INTERNAL = 8     /* device: an internal consistency check failed (a bug); the write was skipped */
 } dsa_status;
 
 /* One call's batch.  q_off and ctx_len are DEVICE int32 arrays so that a

@@ -27,7 +27,7 @@ H_IDX, D_IDX, H, D_QK, D_V, MAX_TOPK = 32, 128, 64, 576, 512, 2048
 
 STATUS = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
-    4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_BAD_BATCH", 7: "DSA_ERR_BAD_INDEX",
+    4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_BAD_BATCH", 7: "DSA_ERR_BAD_INDEX", 8: "DSA_ERR_INTERNAL",
 }
 
 EXPORTS = ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",

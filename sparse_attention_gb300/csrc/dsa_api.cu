@@ -97,6 +97,7 @@ const char* dsa_status_string(int s) {
         case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: a bounded in-kernel wait expired";
         case DSA_ERR_BAD_BATCH: return "DSA_ERR_BAD_BATCH: q_off/ctx_len outside the host bounds";
         case DSA_ERR_BAD_INDEX: return "DSA_ERR_BAD_INDEX: a selected index outside [-1, t]";
+        case DSA_ERR_INTERNAL: return "DSA_ERR_INTERNAL: an internal consistency check failed in a kernel";
         default: return "unknown dsa_status";
     }
 }

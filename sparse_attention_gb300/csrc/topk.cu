@@ -162,6 +162,13 @@ __device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, int c
     }
 }
 
+// out[pos] = v for a rank pos < k; a rank outside the row would be a bug:
+// it is skipped and latched instead of written.
+__device__ __forceinline__ void put(int32_t* out, uint32_t pos, int k, int32_t v, int32_t* status) {
+    if (pos < (uint32_t)k) out[pos] = v;
+    else latch_status(status, DSA_ERR_INTERNAL);
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
     topk_kernel(const BatchDev bd, const RowRange rr, const float* __restrict__ scores, const int64_t ld,
                 const int scores_local, const int k, int32_t* __restrict__ idx, const int idx_local,
@@ -306,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool isg = s < c && key > tau, ise = s < c && key == tau;
             const uint32_t bg = __ballot_sync(0xffffffffu, isg), be = __ballot_sync(0xffffffffu, ise);
             const uint32_t gtb = gt_run + __popc(bg & lower), eqb = eq_run + __popc(be & lower);
-            if (isg) out[gtb + min(eqb, need)] = rp[s];
-            else if (ise && eqb < need) out[gtb + eqb] = rp[s];
+            if (isg) put(out, gtb + min(eqb, need), k, rp[s], status);
+            else if (ise && eqb < need) put(out, gtb + eqb, k, rp[s], status);
             gt_run += __popc(bg);
             eq_run += __popc(be);
         }
@@ -370,10 +377,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int x = 0; x < kE; ++x) {
                 if (j0 + x < len) {
                     if (kk[x] > tau) {
-                        out[gtb + min(eqb, need)] = s_lo + j0 + x;
+                        put(out, gtb + min(eqb, need), k, s_lo + j0 + x, status);
                         ++gtb;
                     } else if (kk[x] == tau) {
-                        if (eqb < need) out[gtb + eqb] = s_lo + j0 + x;
+                        if (eqb < need) put(out, gtb + eqb, k, s_lo + j0 + x, status);
                         ++eqb;
                     }
                 }
