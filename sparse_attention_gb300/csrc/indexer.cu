@@ -14,10 +14,11 @@
 //               a ring of shared-memory stages (128B-swizzled boxes)
 //   warp 1      TMEM allocator and MMA issuer (tcgen05.mma kind::f16,
 //               bf16 x bf16 -> fp32), double-buffered accumulators
-//   warps 2..5  epilogue: tcgen05.ld one key row per thread, then the ReLU
-//               and the head-weighted sum in registers (fp32, heads in
-//               order), and a coalesced store of one fp32 score per
-//               (query, key) with s <= t.
+//   warps 2..5  epilogue: tcgen05.ld one key row per thread (two queries'
+//               accumulators per wait), then the ReLU and the
+//               head-weighted sum in registers (fp32, four partial sums
+//               over the heads in a fixed order), and a coalesced store of
+//               one fp32 score per (query, key) with s <= t.
 // Scores of positions s > t are never written.
 #include <cuda.h>
 
@@ -42,6 +43,7 @@ struct IdxCfg {
     static constexpr int kAcc = 2;                   // TMEM accumulator buffers
     static constexpr int kTmemCols = (kN * kAcc < 32) ? 32 : kN * kAcc;
     static constexpr int kThreads = 192;
+    static constexpr int kEpiQ = (NQ >= 2) ? 2 : 1;    // queries read from TMEM per wait
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
     static constexpr int kOffW = kOffB + kBBytes;
@@ -62,6 +64,7 @@ __global__ void __launch_bounds__(192, 1)
                    float* __restrict__ scores, const int64_t ld, const int scores_local,
                    const int tiles_per_split, int32_t* status) {
     using C = IdxCfg<NQ>;
+    constexpr int kEpiQ = C::kEpiQ;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -207,18 +210,30 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_after();
             const int32_t s = (j0 + it) * C::kBM + row;
+            const uint32_t tq = tmem_base + ((lq * 32u) << 16) + (uint32_t)(a * C::kN);
 #pragma unroll 1
-            for (int qi = 0; qi < NQ; ++qi) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + ((lq * 32u) << 16) + (uint32_t)(a * C::kN + qi * 32), r);
-                tmem_ld_wait();
-                const int32_t i = qlo + qi;
-                if (i < qhi) {
-                    const float* wq = w_s + qi * kHIdx;
-                    float acc = 0.f;
+            for (int q0 = 0; q0 < NQ; q0 += kEpiQ) {
+                // kEpiQ queries' accumulators in flight before one wait
+                uint32_t r[kEpiQ][32];
 #pragma unroll
-                    for (int h = 0; h < kHIdx; ++h) acc = fmaf(wq[h], fmaxf(__uint_as_float(r[h]), 0.f), acc);
-                    if (s <= pos0 + i) scores[buf_row(scores_local, sq, b, i, rr) * ld + s] = acc;
+                for (int u = 0; u < kEpiQ; ++u) tmem_ld_32x32b_x32(tq + (uint32_t)((q0 + u) * 32), r[u]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < kEpiQ; ++u) {
+                    const int32_t i = qlo + q0 + u;
+                    const float4* wq = reinterpret_cast<const float4*>(w_s + (q0 + u) * kHIdx);
+                    // four partial sums over heads h = 4m + j, m in order, then (a0 + a1) + (a2 + a3)
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int m = 0; m < kHIdx / 4; ++m) {
+                        const float4 wv = wq[m];
+                        acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(r[u][4 * m]), 0.f), acc[0]);
+                        acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(r[u][4 * m + 1]), 0.f), acc[1]);
+                        acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(r[u][4 * m + 2]), 0.f), acc[2]);
+                        acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(r[u][4 * m + 3]), 0.f), acc[3]);
+                    }
+                    const float v = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                    if (i < qhi && s <= pos0 + i) scores[buf_row(scores_local, sq, b, i, rr) * ld + s] = v;
                 }
             }
             tc_fence_before();

@@ -235,3 +235,27 @@ def test_indexshare_window_reuses_the_full_layers_indices():
         out, lse = sl.attention(idx)
         check_attention(sl, idx, out, lse)          # the shared layer against the oracle on the reused indices
         assert sl.status() == 0
+
+
+def test_chunked_equals_one_call():
+    # chunked prefill: the queries of one sequence in chunks of 1000 rows
+    # (not a multiple of the 8-query group, so the groups fall differently
+    # than in one call), each chunk against the cache written so far
+    T, C, k = 2600, 1000, 256
+    full = W.make_batch_np([T], [T], k=k, seed=83, key_kind="lowrank16")
+    st = Staged(full)
+    out_all, lse_all, idx_all, _ = st.forward()
+    check_attention(st, idx_all, out_all, lse_all, rows=[0, 999, 1000, 1001, 2599])
+    for c0 in range(0, T, C):
+        n = min(C, T - c0)
+        b = dsa.make_batch([0, n], [c0 + n], n, c0 + n, T)
+        ws = dsa.workspace(b, k)
+        out = torch.empty((n, 64, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((n, 64), dtype=torch.float32, device="cuda")
+        idx = torch.empty((n, k), dtype=torch.int32, device="cuda")
+        s = slice(c0, c0 + n)
+        dsa.forward(b, st.q_idx[s], st.w[s], st.k_idx, st.q[s], st.kv, k, full.sm_scale, out, lse, idx_out=idx,
+                    ws=ws)
+        assert dsa.read_device_status(ws) == 0
+        assert torch.equal(idx, idx_all[s])
+        assert torch.equal(out.view(torch.int16), out_all[s].view(torch.int16)) and torch.equal(lse, lse_all[s])
