@@ -134,6 +134,11 @@ __global__ void __launch_bounds__(192, 1)
             mbar_arrive_expect_tx(bfull_bar, C::kBBytes);
             tma_load_2d(sB, &tm_q, bfull_bar, 0, qrow);
             tma_load_2d(sB + C::kBBoxBytes, &tm_q, bfull_bar, 64, qrow);
+            // one query group per sequence: every key is read by one CTA only,
+            // so the stream is marked evict-first and the scores produced
+            // from it stay in L2 for the top-k
+            const bool once = bd.max_q <= NQ;
+            const uint64_t pol = l2_evict_first_policy();
             int issued = 0;
             for (int it = 0; it < niter; ++it) {
                 const int s = it % C::kStages;
@@ -145,8 +150,13 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 const int32_t krow = (int32_t)((int64_t)b * bd.stride + (int64_t)(j0 + it) * C::kBM);
                 mbar_arrive_expect_tx(full_bar(s), C::kABytes);
-                tma_load_2d(sA + s * C::kABytes, &tm_k, full_bar(s), 0, krow);
-                tma_load_2d(sA + s * C::kABytes + C::kABoxBytes, &tm_k, full_bar(s), 64, krow);
+                if (once) {
+                    tma_load_2d_hint(sA + s * C::kABytes, &tm_k, full_bar(s), 0, krow, pol);
+                    tma_load_2d_hint(sA + s * C::kABytes + C::kABoxBytes, &tm_k, full_bar(s), 64, krow, pol);
+                } else {
+                    tma_load_2d(sA + s * C::kABytes, &tm_k, full_bar(s), 0, krow);
+                    tma_load_2d(sA + s * C::kABytes + C::kABoxBytes, &tm_k, full_bar(s), 64, krow);
+                }
                 ++issued;
             }
             if (misc[1]) {

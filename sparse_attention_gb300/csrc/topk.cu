@@ -9,14 +9,17 @@
 // long and few); CTA r owns the r-th contiguous slice of the row.  Scores
 // map to order-preserving 32-bit keys (-0.0 folded onto +0.0).
 //   1. A lower bound L for the k-th largest key: the lower edge of the
-//      leading-digit bin (top 11 bits) holding the (r+1)-th largest of 1024
-//      evenly spaced keys of the whole row, r sized so that well over k keys
-//      lie at or above it.  Every CTA of the cluster derives the same L.
+//      11-bit digit bin (the digit just below the bits all sampled keys
+//      share) holding the (r+1)-th largest of 1024 evenly spaced keys of the
+//      whole row, r sized so that well over k keys lie at or above it.
+//      Every CTA of the cluster derives the same L.
 //   2. One pass over the slice (16-byte loads, several in flight): warp w of
 //      a CTA owns a contiguous segment and appends its keys >= L, in
-//      position order, to a shared-memory region of its own.
+//      position order, to a shared-memory region of its own (lane l takes
+//      24 consecutive keys per step, one warp scan places them).
 //   3. The exact k-th largest key tau among the candidates of the cluster:
-//      a radix select over three digits (11 + 11 + 10 bits); each CTA counts
+//      a radix select over the bits below those that L and the largest
+//      candidate share (digits of up to 11 bits); each CTA counts
 //      its candidates and every CTA sums the cluster's histograms through
 //      distributed shared memory, so all derive the same digits.
 //   4. The output in position order: candidates above tau and the first
@@ -73,30 +76,35 @@ struct alignas(16) TopkSmem {
     uint32_t cand_key[kMaxCand];          // warp w: [w * kRegion, w * kRegion + count)
     int32_t cand_pos[kMaxCand];
     uint32_t warp_sums[32];
-    uint32_t wcnt[32], wgt[32], weq[32];
+    uint32_t wcnt[32], wgt[32], weq[32], wmax[32];
     uint32_t total, sel_digit, sel_above, chunk_total;
-    uint32_t cta_cand, cta_overflow, cta_gt, cta_eq;   // read by the rest of the cluster
+    uint32_t cta_cand, cta_overflow, cta_gt, cta_eq, cta_max;   // read by the rest of the cluster
 };
 
-// The k-th largest of the keys j in [0, m) with valid_of(j), over this CTA
-// (nranks == 1) or over the whole cluster (nranks == cluster size), resolved
-// to the first `passes` digits (3 = exact): returns tau (the digits found,
+// The k-th largest of the keys that `visit` hands to this thread's callback,
+// over this CTA (nranks == 1) or over the whole cluster (nranks == cluster
+// size).  Every such key agrees with `prefix0` above its low `hi` bits;
+// those bits are resolved from the top in digits of up to 11 bits, at most
+// `passes` of them (enough passes = exact).  Returns tau (the bits found,
 // zero below) and sets need = how many keys matching tau belong to the top
-// k.  S.hist must be zero on entry; zero on return.
-template <typename KeyOf, typename ValidOf>
-__device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSmem& S, int32_t m, uint32_t k,
-                                 int passes, KeyOf key_of, ValidOf valid_of, uint32_t& need_out) {
+// k.  Starting below the bits the keys share keeps them spread over many
+// bins (few atomic collisions).  S.hist must be zero on entry; zero on
+// return.
+template <typename Visit>
+__device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSmem& S, uint32_t k, int hi,
+                                 uint32_t prefix0, int passes, Visit visit, uint32_t& need_out) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t prefix = 0u, pmask = 0u, need = k;
+    uint32_t pmask = hi >= 32 ? 0u : ~((1u << hi) - 1u);
+    uint32_t prefix = prefix0 & pmask, need = k;
+    int top = hi;
 #pragma unroll 1
-    for (int p = 0; p < passes; ++p) {
-        const int sh = p == 0 ? 21 : (p == 1 ? 10 : 0);
-        const uint32_t dmask = p == 2 ? 0x3FFu : 0x7FFu;
-        for (int32_t j = tid; j < m; j += kThreads) {
-            if (!valid_of(j)) continue;
-            const uint32_t key = key_of(j);
+    for (int p = 0; p < passes && top > 0; ++p) {
+        const int sh = max(0, top - 11);
+        const uint32_t dmask = (1u << (top - sh)) - 1u;
+        top = sh;
+        visit([&](uint32_t key) {
             if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> sh) & dmask], 1u);
-        }
+        });
         // thread tid owns bins [4 tid, 4 tid + 4), summed over the ranks
         uint32_t c[kBinsPerThread];
         uint32_t mine = 0u;
@@ -149,6 +157,11 @@ __device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSme
     return prefix;
 }
 
+// Number of low bits in which keys of [lo, hi] may differ.
+__device__ __forceinline__ int varying_bits(uint32_t lo, uint32_t hi) {
+    return lo == hi ? 0 : 32 - __clz((int)(lo ^ hi));
+}
+
 // Exclusive prefix over the cluster's lower ranks of the CTA counts (gt, eq)
 // stored in S.cta_gt / S.cta_eq; call after a cluster barrier.
 __device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, int crank, TopkSmem& S, uint32_t& gt0,
@@ -190,6 +203,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float* row = scores + buf_row(scores_local, sq, b, i, rr) * ld;
     int32_t* out = idx + buf_row(idx_local, sq, b, i, rr) * (int64_t)k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // a barrier over every thread that shares this row
+    auto sync_row = [&]() {
+        if (csize == 1) __syncthreads();
+        else cluster.sync();
+    };
 
     if (n <= k) {  // every causal position is selected
         if (crank == 0)
@@ -202,79 +220,121 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int32_t span = ((n + csize - 1) / csize + 127) & ~127;
     const int32_t s_lo = min(n, crank * span), s_hi = min(n, s_lo + span);
 
-    // 1. the lower bound L (the same in every CTA)
+    // 1. the lower bound L (the same in every CTA): digits start below the
+    // bits that all sample keys share
     const int32_t ns = min(n, kSample);
 #pragma unroll
     for (int x = 0; x < kBinsPerThread; ++x) S.hist[kBinsPerThread * tid + x] = 0u;
-    for (int q = tid; q < ns; q += kThreads) S.sample[q] = row_key((int32_t)(((int64_t)q * n) / ns));
+    uint32_t smin = 0xFFFFFFFFu, smax = 0u;
+    for (int q = tid; q < ns; q += kThreads) {
+        const uint32_t key = row_key((int32_t)(((int64_t)q * n) / ns));
+        S.sample[q] = key;
+        smin = min(smin, key);
+        smax = max(smax, key);
+    }
+    smin = __reduce_min_sync(0xffffffffu, smin);
+    smax = __reduce_max_sync(0xffffffffu, smax);
+    if (lane == 0) {
+        S.wgt[warp] = smin;
+        S.weq[warp] = smax;
+    }
     __syncthreads();
+    smin = __reduce_min_sync(0xffffffffu, lane < kWarps ? S.wgt[lane] : 0xFFFFFFFFu);
+    smax = __reduce_max_sync(0xffffffffu, lane < kWarps ? S.weq[lane] : 0u);
     const float expect = (float)k * (float)ns / (float)n;
     const int32_t r = min(ns - 1, (int32_t)(1.25f * expect + 3.f * sqrtf(expect)) + 8);
     uint32_t unused;
-    const uint32_t L = radix_select(cluster, 1, S, ns, (uint32_t)(r + 1), 1, [&](int32_t j) { return S.sample[j]; },
-                                    [](int32_t) { return true; }, unused);
+    const uint32_t L = radix_select(cluster, 1, S, (uint32_t)(r + 1), varying_bits(smin, smax), smin, 1,
+                                    [&](auto&& f) {
+                                        for (int q = tid; q < ns; q += kThreads) f(S.sample[q]);
+                                    },
+                                    unused);
 
-    // 2. one pass: warp w appends its keys >= L to its region, in order
+    // 2. one pass: warp w appends its keys >= L to its region, in position
+    // order; lane l of a warp takes 24 consecutive keys (6 16-byte loads in
+    // flight), so one scan over the lanes orders the whole step
     const int32_t seg = ((s_hi - s_lo + kWarps - 1) / kWarps + 127) & ~127;
     const int32_t w_lo = min(s_hi, s_lo + warp * seg), w_hi = min(s_hi, w_lo + seg);
     uint32_t* rk = S.cand_key + warp * kRegion;
     int32_t* rp = S.cand_pos + warp * kRegion;
-    uint32_t cnt = 0u;
-    for (int32_t jb = w_lo; jb < w_hi; jb += 128 * kPrefetch) {
+    uint32_t cnt = 0u, cmax = 0u;
+    constexpr int kLaneKeys = 4 * kPrefetch;
+    for (int32_t jb = w_lo; jb < w_hi; jb += 32 * kLaneKeys) {
+        const int32_t j0 = jb + kLaneKeys * lane;       // a multiple of 4 inside the padded row
         float4 v[kPrefetch];
 #pragma unroll
         for (int u = 0; u < kPrefetch; ++u) {       // all loads in flight before any use
-            const int32_t j = jb + 128 * u + 4 * lane;
+            const int32_t j = j0 + 4 * u;
             v[u] = j < w_hi ? __ldg(reinterpret_cast<const float4*>(row + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        uint32_t kk[kLaneKeys];
+        uint32_t mine = 0u;
 #pragma unroll
         for (int u = 0; u < kPrefetch; ++u) {
-            const int32_t j = jb + 128 * u + 4 * lane;   // a multiple of 4 inside the padded row
-            const uint32_t kk[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w)};
-            uint32_t mine = 0u;
+            kk[4 * u] = order_key(v[u].x);
+            kk[4 * u + 1] = order_key(v[u].y);
+            kk[4 * u + 2] = order_key(v[u].z);
+            kk[4 * u + 3] = order_key(v[u].w);
+        }
 #pragma unroll
-            for (int x = 0; x < 4; ++x) mine += (j + x < w_hi && kk[x] >= L) ? 1u : 0u;
-            const uint32_t incl = warp_inclusive_scan(mine);
+        for (int x = 0; x < kLaneKeys; ++x) {
+            const bool c = j0 + x < w_hi && kk[x] >= L;
+            mine += c ? 1u : 0u;
+            cmax = c ? max(cmax, kk[x]) : cmax;
+        }
+        const uint32_t incl = warp_inclusive_scan(mine);
+        if (mine) {
             uint32_t at = cnt + incl - mine;
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                if (j + x < w_hi && kk[x] >= L) {
+            for (int x = 0; x < kLaneKeys; ++x) {
+                if (j0 + x < w_hi && kk[x] >= L) {
                     if (at < (uint32_t)kRegion) {
                         rk[at] = kk[x];
-                        rp[at] = j + x;
+                        rp[at] = j0 + x;
                     }
                     ++at;
                 }
             }
-            cnt += __shfl_sync(0xffffffffu, incl, 31);
         }
+        cnt += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) S.wcnt[warp] = cnt;
+    cmax = __reduce_max_sync(0xffffffffu, cmax);
+    if (lane == 0) {
+        S.wcnt[warp] = cnt;
+        S.wmax[warp] = cmax;
+    }
     __syncthreads();
     if (warp == 0) {
         const uint32_t c = lane < kWarps ? S.wcnt[lane] : 0u;
         const uint32_t tot = warp_inclusive_scan(c);
         const bool overflow = __any_sync(0xffffffffu, c > (uint32_t)kRegion);
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, lane < kWarps ? S.wmax[lane] : 0u);
         if (lane == 31) {
             S.cta_cand = tot;
             S.cta_overflow = overflow ? 1u : 0u;
+            S.cta_max = mx;
         }
     }
-    cluster.sync();
-    uint32_t all_cand = 0u, any_overflow = 0u;
+    sync_row();
+    uint32_t all_cand = 0u, any_overflow = 0u, all_max = 0u;
     for (int q = 0; q < csize; ++q) {
-        const TopkSmem* o = cluster.map_shared_rank(&S, q);
+        const TopkSmem* o = csize == 1 ? &S : cluster.map_shared_rank(&S, q);
         all_cand += o->cta_cand;
         any_overflow |= o->cta_overflow;
+        all_max = max(all_max, o->cta_max);
     }
     const bool use_candidates = !any_overflow && all_cand >= (uint32_t)k;
 
     uint32_t need;
     if (use_candidates) {
-        // 3. tau among the cluster's candidates (slots past a count are empty)
-        const uint32_t tau = radix_select(
-            cluster, csize, S, kMaxCand, (uint32_t)k, 3, [&](int32_t j) { return S.cand_key[j]; },
-            [&](int32_t j) { return (uint32_t)(j % kRegion) < S.wcnt[j / kRegion]; }, need);
+        // 3. tau among the cluster's candidates; every candidate lies in
+        // [L, all_max], so the bits the two share are known
+        const uint32_t tau = radix_select(cluster, csize, S, (uint32_t)k, varying_bits(L, all_max), L, 3,
+                                          [&](auto&& f) {
+                                              const uint32_t c = S.wcnt[warp];
+                                              for (uint32_t s = lane; s < c; s += 32) f(rk[s]);
+                                          },
+                                          need);
         // 4. ordered output: counts per warp, prefix over warps and lower CTAs
         const uint32_t c = S.wcnt[warp];
         uint32_t g = 0u, e = 0u;
@@ -302,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 S.cta_eq = ei;
             }
         }
-        cluster.sync();
+        sync_row();
         uint32_t gt0, eq0;
         cluster_prefix(cluster, crank, S, gt0, eq0);
         uint32_t gt_run = gt0 + S.wgt[warp], eq_run = eq0 + S.weq[warp];
@@ -322,8 +382,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         // the sample misjudged: select and write over the whole slices
         const int32_t len = s_hi - s_lo;
         auto slice_key = [&](int32_t j) -> uint32_t { return row_key(s_lo + j); };
-        const uint32_t tau =
-            radix_select(cluster, csize, S, len, (uint32_t)k, 3, slice_key, [](int32_t) { return true; }, need);
+        const uint32_t tau = radix_select(cluster, csize, S, (uint32_t)k, 32, 0u, 3,
+                                          [&](auto&& f) {
+                                              for (int32_t j = tid; j < len; j += kThreads) f(slice_key(j));
+                                          },
+                                          need);
         uint32_t g = 0u, e = 0u;
         for (int32_t j = tid; j < len; j += kThreads) {
             const uint32_t key = slice_key(j);
@@ -344,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 S.cta_eq = es;
             }
         }
-        cluster.sync();
+        sync_row();
         uint32_t gt_run, eq_run;
         cluster_prefix(cluster, crank, S, gt_run, eq_run);
         constexpr int kE = 4;
@@ -390,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncthreads();
         }
     }
-    cluster.sync();                                // the cluster may still read this CTA's counts
+    if (csize > 1) cluster.sync();                 // the cluster may still read this CTA's counts
 }
 
 }  // namespace
