@@ -15,8 +15,8 @@
 //      Every CTA of the cluster derives the same L.
 //   2. One pass over the slice (16-byte loads, several in flight): warp w of
 //      a CTA owns a contiguous segment and appends its keys >= L, in
-//      position order, to a shared-memory region of its own (lane l takes
-//      24 consecutive keys per step, one warp scan places them).
+//      position order, to a shared-memory region of its own (keys are
+//      tested as floats against L; one warp scan per step places them).
 //   3. The exact k-th largest key tau among the candidates of the cluster:
 //      a radix select over the bits below those that L and the largest
 //      candidate share (digits of up to 11 bits); each CTA counts
@@ -42,14 +42,13 @@ namespace cg = cooperative_groups;
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 512;                // two CTAs per SM
-constexpr int kWarps = kThreads / 32;
+// Threads per CTA: 1024 when a launch has fewer rows than SMs (one CTA per
+// SM, more warps to hide latency), else 512 (two CTAs per SM).
 constexpr int kBins = 2048;
-constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kSample = 1024;
 constexpr int kRegion = 512;                 // candidate slots per warp
-constexpr int kMaxCand = kWarps * kRegion;   // 8192 per CTA
-constexpr int kPrefetch = 6;                 // 16-byte loads in flight per lane
+constexpr int kPrefetch = 8;                 // 16-byte loads in flight per lane (32 keys)
+static_assert(kPrefetch <= 8, "a lane's candidate flags fill one 32-bit word, its counts one 64-bit word");
 constexpr int kMaxCluster = 8;
 constexpr int kLongRow = 65536;              // rows above this may be split over a cluster
 constexpr int kKeysPerCta = 32768;
@@ -58,6 +57,13 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
     if (u == 0x80000000u) u = 0u;     // -0.0 compares equal to +0.0
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The float whose key is `key` (inverse of order_key; +0.0 for the key of
+// zero).  For non-NaN x: x >= key_float(key) exactly when order_key(x) >= key,
+// provided key_float(key) is not a NaN.
+__device__ __forceinline__ float key_float(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 __device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
@@ -70,14 +76,19 @@ __device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
     return v;
 }
 
+template <int NT>
 struct alignas(16) TopkSmem {
+    static constexpr int kMaxCand = NT / 32 * kRegion;
     uint32_t hist[kBins];                 // zero between selects
     uint32_t sample[kSample];
     uint32_t cand_key[kMaxCand];          // warp w: [w * kRegion, w * kRegion + count)
     int32_t cand_pos[kMaxCand];
     uint32_t warp_sums[32];
     uint32_t wcnt[32], wgt[32], weq[32], wmax[32];
-    uint32_t total, sel_digit, sel_above, chunk_total;
+    uint32_t small[64];                   // this CTA's keys of a small boundary bin
+    uint32_t small_all[64];               // the bin's keys of the whole cluster
+    uint32_t total, sel_digit, sel_above, sel_count, chunk_total;
+    uint32_t small_n, small_all_n, small_tau, small_need;
     uint32_t cta_cand, cta_overflow, cta_gt, cta_eq, cta_max;   // read by the rest of the cluster
 };
 
@@ -88,11 +99,13 @@ struct alignas(16) TopkSmem {
 // `passes` of them (enough passes = exact).  Returns tau (the bits found,
 // zero below) and sets need = how many keys matching tau belong to the top
 // k.  Starting below the bits the keys share keeps them spread over many
-// bins (few atomic collisions).  S.hist must be zero on entry; zero on
-// return.
-template <typename Visit>
-__device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSmem& S, uint32_t k, int hi,
+// bins (few atomic collisions).  Once at most 64 keys (over the cluster)
+// remain in the boundary bin, they are gathered and ranked directly.  S.hist must
+// be zero on entry; zero on return.
+template <int NT, typename Visit>
+__device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSmem<NT>& S, uint32_t k, int hi,
                                  uint32_t prefix0, int passes, Visit visit, uint32_t& need_out) {
+    constexpr int kWarps = NT / 32, kBinsPerThread = kBins / NT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t pmask = hi >= 32 ? 0u : ~((1u << hi) - 1u);
     uint32_t prefix = prefix0 & pmask, need = k;
@@ -145,6 +158,7 @@ __device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSme
             if (above < need && need <= above + c[x]) {
                 S.sel_digit = (uint32_t)(kBinsPerThread * tid + x);
                 S.sel_above = above;
+                S.sel_count = c[x];
             }
             above += c[x];
         }
@@ -152,6 +166,69 @@ __device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSme
         need -= S.sel_above;
         prefix |= S.sel_digit << sh;
         pmask |= dmask << sh;
+        if (passes > 1 && top > 0 && S.sel_count <= 64u) {
+            // at most 64 keys (in the cluster) share the digits found so far:
+            // gather them and rank them exactly instead of more passes
+            if (tid == 0) S.small_n = 0u;
+            __syncthreads();
+            visit([&](uint32_t key) {
+                if ((key & pmask) == prefix) {
+                    const uint32_t at = atomicAdd(&S.small_n, 1u);
+                    if (at < 64u) S.small[at] = key;
+                }
+            });
+            if (nranks == 1) __syncthreads();
+            else cluster.sync();
+            // every rank's list, concatenated in rank order
+            auto rank_smem = [&](int r) -> const TopkSmem<NT>* {
+                return nranks == 1 ? &S : cluster.map_shared_rank(&S, r);
+            };
+            if (tid < 64 * nranks) {
+                const int r = tid >> 6, e = tid & 63;
+                const TopkSmem<NT>* o = rank_smem(r);
+                if ((uint32_t)e < min(o->small_n, 64u)) {
+                    uint32_t off = 0u;
+                    for (int r2 = 0; r2 < r; ++r2) off += min(rank_smem(r2)->small_n, 64u);
+                    if (off + (uint32_t)e < 64u) S.small_all[off + e] = o->small[e];
+                }
+            }
+            if (tid == 0) {
+                uint32_t tot = 0u;
+                for (int r2 = 0; r2 < nranks; ++r2) tot += min(rank_smem(r2)->small_n, 64u);
+                S.small_all_n = min(tot, 64u);
+            }
+            __syncthreads();
+            // thread t ranks key t / 8 against keys 8 (t % 8) .. 8 (t % 8) + 7;
+            // eight lanes sum their counts
+            if (tid < 512) {
+                const uint32_t nb = S.small_all_n;
+                const uint32_t q = (uint32_t)tid >> 3, sub = (uint32_t)tid & 7u;
+                const uint32_t x = q < nb ? S.small_all[q] : 0u;
+                uint32_t gt = 0u, eq = 0u;
+#pragma unroll
+                for (uint32_t o = 0; o < 8u; ++o) {
+                    const uint32_t qq = sub * 8u + o;
+                    const uint32_t y = S.small_all[qq];
+                    gt += (qq < nb && y > x) ? 1u : 0u;
+                    eq += (qq < nb && y == x) ? 1u : 0u;
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    gt += __shfl_xor_sync(0xffffffffu, gt, o);
+                    eq += __shfl_xor_sync(0xffffffffu, eq, o);
+                }
+                // tau: the key with fewer than `need` larger keys and at least
+                // `need` keys at or above it (every such thread agrees)
+                if (sub == 0 && q < nb && gt < need && need <= gt + eq) {
+                    S.small_tau = x;
+                    S.small_need = need - gt;
+                }
+            }
+            __syncthreads();
+            prefix = S.small_tau;
+            need = S.small_need;
+            break;
+        }
     }
     need_out = need;
     return prefix;
@@ -164,12 +241,13 @@ __device__ __forceinline__ int varying_bits(uint32_t lo, uint32_t hi) {
 
 // Exclusive prefix over the cluster's lower ranks of the CTA counts (gt, eq)
 // stored in S.cta_gt / S.cta_eq; call after a cluster barrier.
-__device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, int crank, TopkSmem& S, uint32_t& gt0,
-                                               uint32_t& eq0) {
+template <int NT>
+__device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, int crank, TopkSmem<NT>& S,
+                                               uint32_t& gt0, uint32_t& eq0) {
     gt0 = 0u;
     eq0 = 0u;
     for (int r = 0; r < crank; ++r) {
-        const TopkSmem* o = cluster.map_shared_rank(&S, r);
+        const TopkSmem<NT>* o = cluster.map_shared_rank(&S, r);
         gt0 += o->cta_gt;
         eq0 += o->cta_eq;
     }
@@ -182,12 +260,14 @@ __device__ __forceinline__ void put(int32_t* out, uint32_t pos, int k, int32_t v
     else latch_status(status, DSA_ERR_INTERNAL);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+template <int NT>
+__global__ void __launch_bounds__(NT, NT <= 512 ? 2 : 1)
     topk_kernel(const BatchDev bd, const RowRange rr, const float* __restrict__ scores, const int64_t ld,
                 const int scores_local, const int k, int32_t* __restrict__ idx, const int idx_local,
                 const int csize, int32_t* status) {
+    constexpr int kThreads = NT, kWarps = NT / 32, kBinsPerThread = kBins / NT;
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    TopkSmem& S = *reinterpret_cast<TopkSmem*>(smem_raw);
+    TopkSmem<NT>& S = *reinterpret_cast<TopkSmem<NT>*>(smem_raw);
     cg::cluster_group cluster = cg::this_cluster();
 
     // every test below depends only on the row, so all CTAs of a cluster
@@ -251,53 +331,73 @@ __global__ void __launch_bounds__(kThreads, 2)
                                     unused);
 
     // 2. one pass: warp w appends its keys >= L to its region, in position
-    // order; lane l of a warp takes 24 consecutive keys (6 16-byte loads in
-    // flight), so one scan over the lanes orders the whole step
+    // order.  A step covers 128 x kPrefetch consecutive keys: lane l loads
+    // the 16-byte groups l, l + 32, ... (coalesced, all in flight at once).
+    // Keys are tested as floats against the float of L (the same order as
+    // the keys, -0.0 == +0.0).  The per-group candidate counts of a lane
+    // travel through one 64-bit warp scan (8-bit fields), which places every
+    // candidate of the step in position order; candidates are re-read (L1
+    // hits) to be converted and stored.
     const int32_t seg = ((s_hi - s_lo + kWarps - 1) / kWarps + 127) & ~127;
     const int32_t w_lo = min(s_hi, s_lo + warp * seg), w_hi = min(s_hi, w_lo + seg);
     uint32_t* rk = S.cand_key + warp * kRegion;
     int32_t* rp = S.cand_pos + warp * kRegion;
-    uint32_t cnt = 0u, cmax = 0u;
-    constexpr int kLaneKeys = 4 * kPrefetch;
-    for (int32_t jb = w_lo; jb < w_hi; jb += 32 * kLaneKeys) {
-        const int32_t j0 = jb + kLaneKeys * lane;       // a multiple of 4 inside the padded row
+    const float Lf = key_float(L);
+    uint32_t cnt = 0u;
+    float fmx = -INFINITY;
+    for (int32_t jb = w_lo; jb < w_hi; jb += 128 * kPrefetch) {
         float4 v[kPrefetch];
 #pragma unroll
-        for (int u = 0; u < kPrefetch; ++u) {       // all loads in flight before any use
-            const int32_t j = j0 + 4 * u;
+        for (int u = 0; u < kPrefetch; ++u) {
+            const int32_t j = jb + 128 * u + 4 * (int32_t)lane;   // a multiple of 4 inside the padded row
             v[u] = j < w_hi ? __ldg(reinterpret_cast<const float4*>(row + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        uint32_t kk[kLaneKeys];
-        uint32_t mine = 0u;
+        const bool tail = jb + 128 * kPrefetch > w_hi;    // warp-uniform
+        uint32_t bits = 0u;                               // bit 4u + e: key jb + 128u + 4 lane + e
+        uint64_t packed = 0u;
 #pragma unroll
         for (int u = 0; u < kPrefetch; ++u) {
-            kk[4 * u] = order_key(v[u].x);
-            kk[4 * u + 1] = order_key(v[u].y);
-            kk[4 * u + 2] = order_key(v[u].z);
-            kk[4 * u + 3] = order_key(v[u].w);
-        }
+            float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            uint32_t bu = 0u;
 #pragma unroll
-        for (int x = 0; x < kLaneKeys; ++x) {
-            const bool c = j0 + x < w_hi && kk[x] >= L;
-            mine += c ? 1u : 0u;
-            cmax = c ? max(cmax, kk[x]) : cmax;
-        }
-        const uint32_t incl = warp_inclusive_scan(mine);
-        if (mine) {
-            uint32_t at = cnt + incl - mine;
-#pragma unroll
-            for (int x = 0; x < kLaneKeys; ++x) {
-                if (j0 + x < w_hi && kk[x] >= L) {
-                    if (at < (uint32_t)kRegion) {
-                        rk[at] = kk[x];
-                        rp[at] = j0 + x;
-                    }
-                    ++at;
+            for (int e = 0; e < 4; ++e) {
+                bool c = x[e] >= Lf;
+                if (tail) {
+                    const bool in = jb + 128 * u + 4 * (int32_t)lane + e < w_hi;
+                    c = c && in;
+                    x[e] = in ? x[e] : -INFINITY;        // for the max only
                 }
+                bu |= (c ? 1u : 0u) << e;
+                fmx = fmaxf(fmx, x[e]);
             }
+            bits |= bu << (4 * u);
+            packed |= (uint64_t)__popc(bu) << (8 * u);
         }
-        cnt += __shfl_sync(0xffffffffu, incl, 31);
+        uint64_t incl = packed;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t nb = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += nb;
+        }
+        const uint64_t tot = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t base = cnt;
+#pragma unroll
+        for (int u = 0; u < kPrefetch; ++u) {
+            uint32_t at = base + ((uint32_t)((incl - packed) >> (8 * u)) & 0xFFu);
+            for (uint32_t bb = (bits >> (4 * u)) & 0xFu; bb; bb &= bb - 1u) {
+                const int32_t j = jb + 128 * u + 4 * (int32_t)lane + (int32_t)(__ffs(bb) - 1);
+                if (at < (uint32_t)kRegion) {
+                    rk[at] = row_key(j);
+                    rp[at] = j;
+                }
+                ++at;
+            }
+            base += (uint32_t)(tot >> (8 * u)) & 0xFFu;
+        }
+        cnt = base;
     }
+    // an upper bound of the candidates (keys of the slice, -inf when empty)
+    uint32_t cmax = fmx >= Lf ? order_key(fmx) : 0u;
     cmax = __reduce_max_sync(0xffffffffu, cmax);
     if (lane == 0) {
         S.wcnt[warp] = cnt;
@@ -318,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     sync_row();
     uint32_t all_cand = 0u, any_overflow = 0u, all_max = 0u;
     for (int q = 0; q < csize; ++q) {
-        const TopkSmem* o = csize == 1 ? &S : cluster.map_shared_rank(&S, q);
+        const TopkSmem<NT>* o = csize == 1 ? &S : cluster.map_shared_rank(&S, q);
         all_cand += o->cta_cand;
         any_overflow |= o->cta_overflow;
         all_max = max(all_max, o->cta_max);
@@ -456,6 +556,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (csize > 1) cluster.sync();                 // the cluster may still read this CTA's counts
 }
 
+template <int NT>
+cudaError_t launch_nt(const BatchDev& bd, RowRange rr, const float* scores, int64_t ld, bool scores_local, int k,
+                      int32_t* idx, bool idx_local, int csize, int32_t rows_per_seq, int32_t* status,
+                      cudaStream_t stream) {
+    const size_t smem = sizeof(TopkSmem<NT>);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows_per_seq * csize), (unsigned)bd.B);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, topk_kernel<NT>, bd, rr, scores, ld, scores_local ? 1 : 0, k, idx,
+                           idx_local ? 1 : 0, csize, status);
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, int64_t ld, bool scores_local,
@@ -467,25 +592,10 @@ cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, in
     int csize = 1;
     if (bd.max_ctx > kLongRow && rows < 2 * kNumSMs)
         csize = (int)std::min<int64_t>(kMaxCluster, ((int64_t)bd.max_ctx + kKeysPerCta - 1) / kKeysPerCta);
-    const size_t smem = sizeof(TopkSmem);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(rows_per_seq * csize), (unsigned)bd.B);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, topk_kernel, bd, rr, scores, ld, scores_local ? 1 : 0, k, idx, idx_local ? 1 : 0,
-                           csize, status);
-    if (e == cudaSuccess) count_launches(1);
-    return e;
+    return rows < kNumSMs ? launch_nt<1024>(bd, rr, scores, ld, scores_local, k, idx, idx_local, csize, rows_per_seq,
+                                            status, stream)
+                          : launch_nt<512>(bd, rr, scores, ld, scores_local, k, idx, idx_local, csize, rows_per_seq,
+                                           status, stream);
 }
 
 }  // namespace dsa
