@@ -10,6 +10,9 @@ Functions (all take numpy arrays; bf16 tensors as uint16 bit patterns):
   topk(batch, scores_f32, rows, k)     -> int32   [len(rows), k]
   sparse_mla(batch, idx, rows)         -> (float64 [n, 64, 512], float64 [n, 64])
   masked_mla(batch, idx, rows)         -> same, written in the pages' mask form
+  mla_absorb_q(q_nope, q_pe, w_kvb)    -> float64 [T, 64, 576]
+  mla_output(o_lat, w_kvb, w_o)        -> (float64 [T, 64, 256], float64 [T, 6144])
+  mla_expanded(batch, q_nope, q_pe, w_kvb, w_o, idx, rows) -> same pair, the pages' expanded path
 See ``oracle.c`` for what each computes and the passages it follows.
 """
 
@@ -31,6 +34,7 @@ _lock = threading.Lock()
 _lib = None
 
 H_IDX, D_IDX, H, D_QK, D_V = 32, 128, 64, 576, 512
+D_NOPE, D_ROPE, D_VH, KVB_ROWS, HIDDEN = 192, 64, 256, 64 * 448, 6144
 
 
 def build(force: bool = False) -> str:
@@ -59,6 +63,9 @@ def _load():
             lib.oracle_topk.argtypes = [i32, P, P, P, i64, i32, P, i32, P]
             lib.oracle_sparse_mla.argtypes = [i32, P, P, i64, P, P, P, i32, dbl, i32, P, P, P]
             lib.oracle_masked_mla.argtypes = [i32, P, P, i64, P, P, P, i32, dbl, i32, P, P, P]
+            lib.oracle_mla_absorb_q.argtypes = [i32, P, P, P, P]
+            lib.oracle_mla_output.argtypes = [i32, P, P, P, P, P]
+            lib.oracle_mla_expanded.argtypes = [i32, P, P, i64, P, P, P, P, P, P, i32, dbl, i32, P, P, P]
             _lib = lib
     return _lib
 
@@ -176,3 +183,62 @@ def sparse_mla(batch, idx, rows=None, sm_scale=None):
 def masked_mla(batch, idx, rows=None, sm_scale=None):
     """The same attention in the pages' dense-mask form."""
     return _mla(_load().oracle_masked_mla, batch, idx, rows, sm_scale)
+
+
+def _weights(w_kvb, w_o=None):
+    wk = _np(w_kvb, np.uint16)
+    if wk.size != KVB_ROWS * D_V:
+        raise ValueError(f"kv_b_proj weight holds {wk.size} elements, expected {KVB_ROWS * D_V}")
+    if w_o is None:
+        return wk, None
+    wo = _np(w_o, np.uint16)
+    if wo.size != HIDDEN * H * D_VH:
+        raise ValueError(f"o_proj weight holds {wo.size} elements, expected {HIDDEN * H * D_VH}")
+    return wk, wo
+
+
+def mla_absorb_q(q_nope, q_pe, w_kvb) -> np.ndarray:
+    """The absorbed 576-wide query: [W_UK[h]^T q_nope[h] | q_pe[h]] per head."""
+    qn, qp = _np(q_nope, np.uint16), _np(q_pe, np.uint16)
+    T = qn.size // (H * D_NOPE)
+    if qn.size != T * H * D_NOPE or qp.size != T * H * D_ROPE:
+        raise ValueError("q_nope / q_pe sizes do not match")
+    wk, _ = _weights(w_kvb)
+    out = np.empty((T, H, D_QK), dtype=np.float64)
+    _load().oracle_mla_absorb_q(T, _ptr(qn), _ptr(qp), _ptr(wk), _ptr(out))
+    return out
+
+
+def mla_output(o_lat, w_kvb, w_o) -> Tuple[np.ndarray, np.ndarray]:
+    """Head outputs W_UV[h] o_lat[h] and the o_proj output y."""
+    ol = np.ascontiguousarray(np.asarray(o_lat, dtype=np.float64))
+    T = ol.size // (H * D_V)
+    if ol.size != T * H * D_V:
+        raise ValueError("o_lat size is not a multiple of 64 x 512")
+    wk, wo = _weights(w_kvb, w_o)
+    o_mid = np.empty((T, H, D_VH), dtype=np.float64)
+    y = np.empty((T, HIDDEN), dtype=np.float64)
+    _load().oracle_mla_output(T, _ptr(ol), _ptr(wk), _ptr(wo), _ptr(o_mid), _ptr(y))
+    return o_mid, y
+
+
+def mla_expanded(batch, q_nope, q_pe, w_kvb, w_o, idx, rows=None, sm_scale=None) -> Tuple[np.ndarray, np.ndarray]:
+    """The pages' expanded path (kv_b_proj applied to every attended cached
+    row, masked attention, o_proj) for the given rows and selections."""
+    r = _rows(batch, rows)
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int32))
+    assert idx.ndim == 2 and idx.shape[0] == len(r)
+    qn, qp = _np(q_nope, np.uint16), _np(q_pe, np.uint16)
+    if qn.size < batch.total_q * H * D_NOPE or qp.size < batch.total_q * H * D_ROPE:
+        raise ValueError("q_nope / q_pe hold fewer rows than the batch")
+    kv = _np(batch.kv, np.uint16)
+    _check_layout(batch, kv=kv)
+    wk, wo = _weights(w_kvb, w_o)
+    q_off, ctx = _np(batch.q_off, np.int32), _np(batch.ctx_len, np.int32)
+    scale = float(sm_scale if sm_scale is not None else batch.sm_scale)
+    o_mid = np.empty((len(r), H, D_VH), dtype=np.float64)
+    y = np.empty((len(r), HIDDEN), dtype=np.float64)
+    _load().oracle_mla_expanded(batch.B, _ptr(q_off), _ptr(ctx), int(batch.stride), _ptr(qn), _ptr(qp), _ptr(kv),
+                                _ptr(wk), _ptr(wo), _ptr(idx), idx.shape[1], scale, len(r), _ptr(r), _ptr(o_mid),
+                                _ptr(y))
+    return o_mid, y

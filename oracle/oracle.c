@@ -37,6 +37,23 @@
  *      mask, added to the logits of *every* cached position before the
  *      softmax.  Used to check the gather form against the mask form.
  *
+ * MLA around the path (section 4.5 Steps 1-4 and 7-8; section 4.1: the
+ * cached row is the 512-dim compressed KV after kv_a_layernorm plus the
+ * 64-dim RoPE key; kv_b_proj expands it to 64 heads x (192 nope + 256 v);
+ * o_proj maps the 64 x 256 head outputs to the 6144-dim hidden state):
+ *  oracle_mla_expanded    -- the pages' expanded path for selected rows:
+ *      k_nope = W_UK[h] c, v = W_UV[h] c for every attended cached row
+ *      (W_UK[h], W_UV[h] = rows h*448 .. +191 and h*448+192 .. +447 of
+ *      kv_b_proj's weight), logits sm_scale*(q_nope.k_nope + q_pe.k_pe)
+ *      plus the index mask and the causal mask, softmax, o[h] = sum p v,
+ *      y = o_proj(o).
+ *  oracle_mla_absorb_q    -- the absorbed query: q[h, 0:512] =
+ *      W_UK[h]^T q_nope[h], q[h, 512:576] = q_pe[h] (the identity
+ *      q_nope.(W_UK c) = (W_UK^T q_nope).c moves kv_b_proj's key half onto
+ *      the query, so attention can run on the cached rows directly).
+ *  oracle_mla_output      -- the absorbed output: o[h] = W_UV[h] o_lat[h]
+ *      (sum p (W_UV c) = W_UV sum p c), then y = o_proj(o).
+ *
  * Plain loops, no blocking, no reordering; OpenMP only splits query rows.
  */
 #include <math.h>
@@ -48,6 +65,7 @@
 #endif
 
 enum { O_HIDX = 32, O_DIDX = 128, O_H = 64, O_DQK = 576, O_DV = 512 };
+enum { O_DNOPE = 192, O_DROPE = 64, O_DVH = 256, O_KVB = 448, O_HID = 6144 };
 
 static double widen_bf16(uint16_t b) {
     uint32_t u = ((uint32_t)b) << 16;
@@ -248,5 +266,128 @@ void oracle_masked_mla(int B, const int32_t* q_off, const int32_t* ctx_len, int6
         }
         free(index_mask);
         free(logit);
+    }
+}
+
+/* q_out[t, h, 0:512] = W_UK[h]^T q_nope[t, h]; q_out[t, h, 512:576] = q_pe[t, h]. */
+void oracle_mla_absorb_q(int T, const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* w_kvb,
+                         double* q_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; t++) {
+        for (int h = 0; h < O_H; h++) {
+            double* o = q_out + ((int64_t)t * O_H + h) * O_DQK;
+            for (int d = 0; d < O_DV; d++) o[d] = 0.0;
+            for (int i = 0; i < O_DNOPE; i++) {
+                double qn = widen_bf16(q_nope[((int64_t)t * O_H + h) * O_DNOPE + i]);
+                const uint16_t* wrow = w_kvb + ((int64_t)h * O_KVB + i) * O_DV;
+                for (int d = 0; d < O_DV; d++) o[d] += qn * widen_bf16(wrow[d]);
+            }
+            for (int d = 0; d < O_DROPE; d++)
+                o[O_DV + d] = widen_bf16(q_pe[((int64_t)t * O_H + h) * O_DROPE + d]);
+        }
+    }
+}
+
+/* o_mid[t, h, e] = sum_d W_UV[h][e, d] o_lat[t, h, d];
+ * y[t, n] = sum_{h, e} W_o[n, h*256 + e] o_mid[t, h, e]. */
+void oracle_mla_output(int T, const double* o_lat, const uint16_t* w_kvb, const uint16_t* w_o, double* o_mid,
+                       double* y) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; t++) {
+        double* om = o_mid + (int64_t)t * O_H * O_DVH;
+        for (int h = 0; h < O_H; h++) {
+            const double* ol = o_lat + ((int64_t)t * O_H + h) * O_DV;
+            for (int e = 0; e < O_DVH; e++) {
+                const uint16_t* wrow = w_kvb + ((int64_t)h * O_KVB + O_DNOPE + e) * O_DV;
+                double acc = 0.0;
+                for (int d = 0; d < O_DV; d++) acc += widen_bf16(wrow[d]) * ol[d];
+                om[h * O_DVH + e] = acc;
+            }
+        }
+        for (int n = 0; n < O_HID; n++) {
+            const uint16_t* wrow = w_o + (int64_t)n * (O_H * O_DVH);
+            double acc = 0.0;
+            for (int c = 0; c < O_H * O_DVH; c++) acc += widen_bf16(wrow[c]) * om[c];
+            y[(int64_t)t * O_HID + n] = acc;
+        }
+    }
+}
+
+/* The expanded path for requested rows: every cached position s < ctx_len[b]
+ * gets index_mask[s] + causal[s]; where both are 0 the logit is
+ * sm_scale * (q_nope . k_nope[s] + q_pe . k_pe[s]) with k_nope, v expanded
+ * from the cached latent row by kv_b_proj; elsewhere the logit is -inf (its
+ * finite part does not matter and is not computed).  o_mid[j, h, 0:256],
+ * y[j, 0:6144]. */
+void oracle_mla_expanded(int B, const int32_t* q_off, const int32_t* ctx_len, int64_t stride,
+                         const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* kv, const uint16_t* w_kvb,
+                         const uint16_t* w_o, const int32_t* idx, int k, double sm_scale, int nrows,
+                         const int32_t* rows, double* o_mid, double* y) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int j = 0; j < nrows; j++) {
+        int b;
+        int64_t t;
+        locate_row(B, q_off, ctx_len, rows[j], &b, &t);
+        int64_t ctx = ctx_len[b];
+        double* mask = (double*)malloc((size_t)(ctx > 0 ? ctx : 1) * sizeof(double));
+        double* logit = (double*)malloc((size_t)(ctx > 0 ? ctx : 1) * sizeof(double));
+        double* kn = (double*)malloc(O_DNOPE * sizeof(double));
+        double* v = (double*)malloc(O_DVH * sizeof(double));
+        for (int64_t s = 0; s < ctx; s++) mask[s] = -INFINITY;
+        for (int i = 0; i < k; i++) {
+            int32_t s = idx[(int64_t)j * k + i];
+            if (s >= 0 && s < ctx) mask[s] = 0.0;
+        }
+        double* om = o_mid + (int64_t)j * O_H * O_DVH;
+        for (int h = 0; h < O_H; h++) {
+            const uint16_t* qn = q_nope + ((int64_t)rows[j] * O_H + h) * O_DNOPE;
+            const uint16_t* qp = q_pe + ((int64_t)rows[j] * O_H + h) * O_DROPE;
+            double mx = -INFINITY;
+            for (int64_t s = 0; s < ctx; s++) {
+                double causal = s <= t ? 0.0 : -INFINITY;
+                if (mask[s] + causal < 0.0) {
+                    logit[s] = -INFINITY;
+                    continue;
+                }
+                const uint16_t* row = kv + ((int64_t)b * stride + s) * O_DQK;
+                double dot = 0.0;
+                for (int i = 0; i < O_DNOPE; i++) {
+                    const uint16_t* wrow = w_kvb + ((int64_t)h * O_KVB + i) * O_DV;
+                    double acc = 0.0;
+                    for (int d = 0; d < O_DV; d++) acc += widen_bf16(wrow[d]) * widen_bf16(row[d]);
+                    kn[i] = acc;
+                }
+                for (int i = 0; i < O_DNOPE; i++) dot += widen_bf16(qn[i]) * kn[i];
+                for (int d = 0; d < O_DROPE; d++) dot += widen_bf16(qp[d]) * widen_bf16(row[O_DV + d]);
+                logit[s] = sm_scale * dot + mask[s] + causal;
+                if (logit[s] > mx) mx = logit[s];
+            }
+            for (int e = 0; e < O_DVH; e++) om[h * O_DVH + e] = 0.0;
+            double z = 0.0;
+            for (int64_t s = 0; s < ctx; s++) {
+                if (logit[s] == -INFINITY) continue;
+                const uint16_t* row = kv + ((int64_t)b * stride + s) * O_DQK;
+                double p = exp(logit[s] - mx);
+                z += p;
+                for (int e = 0; e < O_DVH; e++) {
+                    const uint16_t* wrow = w_kvb + ((int64_t)h * O_KVB + O_DNOPE + e) * O_DV;
+                    double acc = 0.0;
+                    for (int d = 0; d < O_DV; d++) acc += widen_bf16(wrow[d]) * widen_bf16(row[d]);
+                    v[e] = acc;
+                }
+                for (int e = 0; e < O_DVH; e++) om[h * O_DVH + e] += p * v[e];
+            }
+            for (int e = 0; e < O_DVH; e++) om[h * O_DVH + e] = z > 0.0 ? om[h * O_DVH + e] / z : 0.0;
+        }
+        for (int n = 0; n < O_HID; n++) {
+            const uint16_t* wrow = w_o + (int64_t)n * (O_H * O_DVH);
+            double acc = 0.0;
+            for (int c = 0; c < O_H * O_DVH; c++) acc += widen_bf16(wrow[c]) * om[c];
+            y[(int64_t)j * O_HID + n] = acc;
+        }
+        free(mask);
+        free(logit);
+        free(kn);
+        free(v);
     }
 }

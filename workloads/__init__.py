@@ -41,6 +41,10 @@ D_V = 512       # kv_lora_rank (V is the latent part of the cached row)
 TOPK = 2048     # index_topk
 SM_SCALE = 1.0 / 16.0   # (192 nope + 64 rope) ** -0.5
 MAX_POS = 202752        # max_position_embeddings
+D_NOPE = 192    # qk_nope_head_dim
+D_ROPE = 64     # qk_rope_head_dim
+D_VH = 256      # v_head_dim
+HIDDEN = 6144   # hidden size (o_proj output)
 
 
 def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
@@ -240,3 +244,49 @@ WORKLOADS: Dict[str, Workload] = {
                                          20264, steps=4),
 }
 
+
+
+# --------------------------------------------------------------------------
+# MLA around the path: un-absorbed queries and random-init projection weights
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class MlaWeights:
+    """kv_b_proj weight [64 * 448, 512] (per head: 192 rows of W_UK, then 256
+    rows of W_UV) and o_proj weight [6144, 64 * 256], bf16 bit patterns
+    (numpy) or bf16 tensors (torch); random init with variance 1/fan_in."""
+    w_kvb: object
+    w_o: object
+
+
+def make_mla_weights_np(seed: int) -> MlaWeights:
+    rng = np.random.default_rng(seed)
+    w_kvb = rng.standard_normal((H * (D_NOPE + D_VH), D_V), dtype=np.float32) / math.sqrt(D_V)
+    w_o = rng.standard_normal((HIDDEN, H * D_VH), dtype=np.float32) / math.sqrt(H * D_VH)
+    return MlaWeights(bf16_bits_from_f32(w_kvb), bf16_bits_from_f32(w_o))
+
+
+def make_mla_weights_torch(seed: int, device: str = "cuda") -> MlaWeights:
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    w_kvb = torch.randn(H * (D_NOPE + D_VH), D_V, generator=g, device=device) / math.sqrt(D_V)
+    w_o = torch.randn(HIDDEN, H * D_VH, generator=g, device=device) / math.sqrt(H * D_VH)
+    return MlaWeights(w_kvb.to(torch.bfloat16), w_o.to(torch.bfloat16))
+
+
+def make_mla_queries_np(total_q: int, seed: int):
+    """q_nope [total_q, 64, 192] and q_pe [total_q, 64, 64] (post-RoPE), bf16 bits."""
+    rng = np.random.default_rng(seed)
+    q_nope = rng.standard_normal((total_q, H, D_NOPE), dtype=np.float32)
+    q_pe = rng.standard_normal((total_q, H, D_ROPE), dtype=np.float32)
+    return bf16_bits_from_f32(q_nope), bf16_bits_from_f32(q_pe)
+
+
+def make_mla_queries_torch(total_q: int, seed: int, device: str = "cuda"):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q_nope = torch.randn(total_q, H, D_NOPE, generator=g, device=device).to(torch.bfloat16)
+    q_pe = torch.randn(total_q, H, D_ROPE, generator=g, device=device).to(torch.bfloat16)
+    return q_nope, q_pe
