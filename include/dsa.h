@@ -69,6 +69,11 @@ extern "C" {
 #define DSA_QK_DIM 576       /* kv_lora_rank 512 + qk_rope_head_dim 64 */
 #define DSA_V_DIM 512        /* kv_lora_rank */
 #define DSA_MAX_TOPK 2048    /* index_topk */
+#define DSA_NOPE_DIM 192     /* qk_nope_head_dim */
+#define DSA_ROPE_DIM 64      /* qk_rope_head_dim */
+#define DSA_V_HEAD_DIM 256   /* v_head_dim */
+#define DSA_KVB_ROWS 448     /* kv_b_proj output rows per head: 192 nope key + 256 value */
+#define DSA_HIDDEN 6144      /* hidden size (o_proj output) */
 
 typedef enum dsa_status {
     DSA_OK = 0,
@@ -203,6 +208,44 @@ DSA_API dsa_status dsa_forward(const dsa_batch* batch, const uint16_t* q_idx, co
                        const uint16_t* k_idx, const uint16_t* q, const uint16_t* kv, int k,
                        float sm_scale, uint16_t* out, float* lse, int32_t* idx_out,
                        float* scores_out, int64_t ld, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- MLA around the path ("GLM-5.1 架构深度拆解", section 4.5 Steps 1-4
+ * and 7-8; section 4.1).  kv_b_proj's weight w_kv_b [64 * 448, 512] holds,
+ * per head h, W_UK[h] (rows h*448 .. h*448+191: k_nope = W_UK[h] c) and
+ * W_UV[h] (rows h*448+192 .. h*448+447: v = W_UV[h] c) for the 512-dim
+ * cached latent c.  Because q_nope . (W_UK c) = (W_UK^T q_nope) . c and
+ * sum_s p_s W_UV c_s = W_UV sum_s p_s c_s, the attention runs on the cached
+ * rows directly: absorb the query before it, apply W_UV and o_proj after. */
+
+/* The absorbed query: q_out[t, h, 0:512] = W_UK[h]^T q_nope[t, h],
+ * q_out[t, h, 512:576] = q_pe[t, h] (bf16, fp32 accumulation, rounded to
+ * nearest even).  Layouts (row-major, DEVICE, bf16 bits, 16-byte aligned):
+ *   q_nope  [total_q, 64, 192]   post-projection query, nope part
+ *   q_pe    [total_q, 64, 64]    post-RoPE query, rope part
+ *   w_kv_b  [64 * 448, 512]      kv_b_proj weight (nn.Linear layout)
+ *   q_out   [total_q, 64, 576]   the q of dsa_sparse_mla_fwd / dsa_forward
+ * ws: any workspace of at least 256 bytes (its status word receives
+ * device-side timeouts).  total_q = 0 is a no-op.  Errors: null or
+ * misaligned pointers, total_q < 0 or >= 2^26 -> DSA_ERR_INVALID_ARG;
+ * launch failures -> DSA_ERR_CUDA. */
+DSA_API dsa_status dsa_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const uint16_t* q_pe,
+                                    const uint16_t* w_kv_b, uint16_t* q_out, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+/* The layer output from the attention's latent output:
+ *   o_mid[t, h*256 + e] = (W_UV[h] o_lat[t, h])[e]     (bf16)
+ *   y[t, n] = sum_c w_o[n, c] o_mid[t, c]              (bf16)
+ * fp32 accumulation, each result rounded to bf16 (o_mid is rounded before
+ * o_proj reads it).  Layouts (row-major, DEVICE, bf16 bits, 16-byte aligned):
+ *   o_lat   [total_q, 64, 512]   `out` of dsa_sparse_mla_fwd / dsa_forward
+ *   w_kv_b  [64 * 448, 512]      kv_b_proj weight
+ *   w_o     [6144, 64 * 256]     o_proj weight (nn.Linear layout)
+ *   o_mid   [total_q, 64 * 256]  caller-owned intermediate
+ *   y       [total_q, 6144]
+ * ws, errors: as dsa_mla_absorb_q. */
+DSA_API dsa_status dsa_mla_output(int32_t total_q, const uint16_t* o_lat, const uint16_t* w_kv_b,
+                                  const uint16_t* w_o, uint16_t* o_mid, uint16_t* y, void* ws, size_t ws_bytes,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

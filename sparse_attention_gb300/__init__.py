@@ -32,7 +32,7 @@ STATUS = {
 
 EXPORTS = ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
            "dsa_selftest_wait_timeout", "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd",
-           "dsa_sparse_mla_fwd_noalloc", "dsa_forward")
+           "dsa_sparse_mla_fwd_noalloc", "dsa_forward", "dsa_mla_absorb_q", "dsa_mla_output")
 
 
 class DsaError(RuntimeError):
@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_sparse_mla_fwd_noalloc.argtypes = [BP, P, P, P, i32, f32, P, P, P, P]
     lib.dsa_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
     lib.dsa_forward.argtypes = [BP, P, P, P, P, P, i32, f32, P, P, P, P, i64, P, sz, P]
+    lib.dsa_mla_absorb_q.argtypes = [i32, P, P, P, P, P, sz, P]
+    lib.dsa_mla_output.argtypes = [i32, P, P, P, P, P, P, sz, P]
     for name in EXPORTS:
         if name not in ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count"):
             getattr(lib, name).restype = ctypes.c_int
@@ -234,3 +236,21 @@ def forward(batch: Batch, q_idx, w, k_idx, q, kv, k: int, sm_scale: float, out, 
                                       int(ld), _p(ws), ws.numel() if ws is not None else 0, _stream(stream)),
            "dsa_forward")
     return out
+
+
+def mla_absorb_q(q_nope, q_pe, w_kv_b, q_out, ws, stream=None):
+    """q_out[t, h] = [W_UK[h]^T q_nope[t, h] | q_pe[t, h]] (see dsa_mla_absorb_q)."""
+    total_q = q_nope.shape[0]
+    assert q_pe.shape[0] == total_q and q_out.shape[0] == total_q
+    _check(load_library().dsa_mla_absorb_q(int(total_q), _bf16(q_nope), _bf16(q_pe), _bf16(w_kv_b), _bf16(q_out),
+                                           _p(ws), ws.numel(), _stream(stream)), "dsa_mla_absorb_q")
+    return q_out
+
+
+def mla_output(o_lat, w_kv_b, w_o, o_mid, y, ws, stream=None):
+    """o_mid[t, h] = W_UV[h] o_lat[t, h]; y[t] = w_o o_mid[t] (see dsa_mla_output)."""
+    total_q = o_lat.shape[0]
+    assert o_mid.shape[0] == total_q and y.shape[0] == total_q
+    _check(load_library().dsa_mla_output(int(total_q), _bf16(o_lat), _bf16(w_kv_b), _bf16(w_o), _bf16(o_mid),
+                                         _bf16(y), _p(ws), ws.numel(), _stream(stream)), "dsa_mla_output")
+    return y

@@ -216,4 +216,27 @@ dsa_status dsa_forward(const dsa_batch* batch, const uint16_t* q_idx, const floa
     return DSA_OK;
 }
 
+dsa_status dsa_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* w_kv_b,
+                            uint16_t* q_out, void* ws, size_t ws_bytes, void* stream) {
+    if (total_q < 0 || total_q >= (1 << 26)) return DSA_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws) || ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
+    if (total_q == 0) return DSA_OK;
+    if (!q_nope || !q_pe || !w_kv_b || !q_out) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(w_kv_b) || !aligned16(q_out)) return DSA_ERR_INVALID_ARG;
+    return cuda_status(launch_mla_absorb_q(total_q, q_nope, q_pe, w_kv_b, q_out, static_cast<int32_t*>(ws),
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_mla_output(int32_t total_q, const uint16_t* o_lat, const uint16_t* w_kv_b, const uint16_t* w_o,
+                          uint16_t* o_mid, uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+    if (total_q < 0 || total_q >= (1 << 26)) return DSA_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws) || ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
+    if (total_q == 0) return DSA_OK;
+    if (!o_lat || !w_kv_b || !w_o || !o_mid || !y) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(o_lat) || !aligned16(w_kv_b) || !aligned16(w_o) || !aligned16(o_mid) || !aligned16(y))
+        return DSA_ERR_INVALID_ARG;
+    return cuda_status(launch_mla_output(total_q, o_lat, w_kv_b, w_o, o_mid, y, static_cast<int32_t*>(ws),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

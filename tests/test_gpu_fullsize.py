@@ -55,6 +55,7 @@ def _check_rows(hb, rows, scores, idx, out, lse):
     rows = list(rows)
     pos = hb.positions()
     ld = scores.shape[1]
+    assert min(rows) >= 0 and max(rows) < scores.shape[0]   # checked on the host before device indexing
     ri = torch.tensor(rows, dtype=torch.long, device=scores.device)
     sc = scores[ri].cpu().numpy()
     ref = oracle.indexer_scores(hb, rows, ld=ld)

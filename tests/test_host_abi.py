@@ -90,6 +90,15 @@ def test_compute_entry_points_reject_bad_host_arguments(lib):
     e = _batch(total_q=0, max_q=0)
     assert lib.dsa_forward(ctypes.byref(e), p, p, p, p, p, 8, ctypes.c_float(0.0625), p, None, None, None, 0,
                            ws, _ws_size(lib, e, 8)[1], None) == 0
+    # MLA projections: bad sizes, missing workspace, null or misaligned pointers
+    assert lib.dsa_mla_absorb_q(-1, p, p, p, p, ws, 256, None) == 1
+    assert lib.dsa_mla_absorb_q(4, p, p, p, p, None, 0, None) == 3
+    assert lib.dsa_mla_absorb_q(4, None, p, p, p, ws, 256, None) == 1
+    assert lib.dsa_mla_absorb_q(4, p, bad, p, p, ws, 256, None) == 1
+    assert lib.dsa_mla_absorb_q(0, None, None, None, None, ws, 256, None) == 0
+    assert lib.dsa_mla_output(1 << 26, p, p, p, p, p, ws, 256, None) == 1
+    assert lib.dsa_mla_output(4, p, p, p, p, None, ws, 256, None) == 1
+    assert lib.dsa_mla_output(4, p, p, p, p, p, ws, 100, None) == 3
     # status word helpers check their pointers on the host
     assert lib.dsa_read_device_status(None, None, None) == 1
     assert lib.dsa_reset_device_status(None, None) == 3
