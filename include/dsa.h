@@ -232,6 +232,13 @@ DSA_API dsa_status dsa_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, con
                                     const uint16_t* w_kv_b, uint16_t* q_out, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* Bytes of workspace dsa_mla_output needs for total_q rows: the 256-byte
+ * status header plus, when few rows leave the tensor cores idle, the fp32
+ * partial sums of a split of the K dimension (summed in a fixed order, so
+ * results do not depend on timing).  Errors: NULL bytes or total_q outside
+ * [0, 2^26) -> DSA_ERR_INVALID_ARG. */
+DSA_API dsa_status dsa_mla_workspace_size(int32_t total_q, size_t* bytes);
+
 /* The layer output from the attention's latent output:
  *   o_mid[t, h*256 + e] = (W_UV[h] o_lat[t, h])[e]     (bf16)
  *   y[t, n] = sum_c w_o[n, c] o_mid[t, c]              (bf16)
@@ -242,7 +249,8 @@ DSA_API dsa_status dsa_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, con
  *   w_o     [6144, 64 * 256]     o_proj weight (nn.Linear layout)
  *   o_mid   [total_q, 64 * 256]  caller-owned intermediate
  *   y       [total_q, 6144]
- * ws, errors: as dsa_mla_absorb_q. */
+ * ws: at least dsa_mla_workspace_size(total_q) bytes, else
+ * DSA_ERR_WORKSPACE; other errors as dsa_mla_absorb_q. */
 DSA_API dsa_status dsa_mla_output(int32_t total_q, const uint16_t* o_lat, const uint16_t* w_kv_b,
                                   const uint16_t* w_o, uint16_t* o_mid, uint16_t* y, void* ws, size_t ws_bytes,
                                   void* stream);

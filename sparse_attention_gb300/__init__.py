@@ -32,7 +32,7 @@ STATUS = {
 
 EXPORTS = ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
            "dsa_selftest_wait_timeout", "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd",
-           "dsa_sparse_mla_fwd_noalloc", "dsa_forward", "dsa_mla_absorb_q", "dsa_mla_output")
+           "dsa_sparse_mla_fwd_noalloc", "dsa_forward", "dsa_mla_absorb_q", "dsa_mla_workspace_size", "dsa_mla_output")
 
 
 class DsaError(RuntimeError):
@@ -81,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_forward.argtypes = [BP, P, P, P, P, P, i32, f32, P, P, P, P, i64, P, sz, P]
     lib.dsa_mla_absorb_q.argtypes = [i32, P, P, P, P, P, sz, P]
     lib.dsa_mla_output.argtypes = [i32, P, P, P, P, P, P, sz, P]
+    lib.dsa_mla_workspace_size.argtypes = [i32, ctypes.POINTER(sz)]
     for name in EXPORTS:
         if name not in ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count"):
             getattr(lib, name).restype = ctypes.c_int
@@ -245,6 +246,15 @@ def mla_absorb_q(q_nope, q_pe, w_kv_b, q_out, ws, stream=None):
     _check(load_library().dsa_mla_absorb_q(int(total_q), _bf16(q_nope), _bf16(q_pe), _bf16(w_kv_b), _bf16(q_out),
                                            _p(ws), ws.numel(), _stream(stream)), "dsa_mla_absorb_q")
     return q_out
+
+
+def mla_workspace(total_q: int, device="cuda") -> torch.Tensor:
+    """A workspace for dsa_mla_output / dsa_mla_absorb_q with a cleared status word."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().dsa_mla_workspace_size(int(total_q), ctypes.byref(n)), "dsa_mla_workspace_size")
+    ws = torch.empty(max(int(n.value), 256), dtype=torch.uint8, device=device)
+    reset_device_status(ws)
+    return ws
 
 
 def mla_output(o_lat, w_kv_b, w_o, o_mid, y, ws, stream=None):

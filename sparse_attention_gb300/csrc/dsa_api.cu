@@ -227,15 +227,22 @@ dsa_status dsa_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const uint1
                                            static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status dsa_mla_workspace_size(int32_t total_q, size_t* bytes) {
+    if (!bytes || total_q < 0 || total_q >= (1 << 26)) return DSA_ERR_INVALID_ARG;
+    *bytes = round_up(kWsHeaderBytes + mla_partial_bytes(total_q), 256);
+    return DSA_OK;
+}
+
 dsa_status dsa_mla_output(int32_t total_q, const uint16_t* o_lat, const uint16_t* w_kv_b, const uint16_t* w_o,
                           uint16_t* o_mid, uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
     if (total_q < 0 || total_q >= (1 << 26)) return DSA_ERR_INVALID_ARG;
-    if (!ws || !aligned16(ws) || ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
+    if (!ws || !aligned16(ws) || ws_bytes < kWsHeaderBytes + mla_partial_bytes(total_q)) return DSA_ERR_WORKSPACE;
     if (total_q == 0) return DSA_OK;
     if (!o_lat || !w_kv_b || !w_o || !o_mid || !y) return DSA_ERR_INVALID_ARG;
     if (!aligned16(o_lat) || !aligned16(w_kv_b) || !aligned16(w_o) || !aligned16(o_mid) || !aligned16(y))
         return DSA_ERR_INVALID_ARG;
-    return cuda_status(launch_mla_output(total_q, o_lat, w_kv_b, w_o, o_mid, y, static_cast<int32_t*>(ws),
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsHeaderBytes);
+    return cuda_status(launch_mla_output(total_q, o_lat, w_kv_b, w_o, o_mid, y, part, static_cast<int32_t*>(ws),
                                          static_cast<cudaStream_t>(stream)));
 }
 

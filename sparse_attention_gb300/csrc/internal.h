@@ -96,6 +96,8 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
 cudaError_t launch_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const uint16_t* q_pe,
                                 const uint16_t* w_kvb, uint16_t* q_out, int32_t* status, cudaStream_t stream);
 cudaError_t launch_mla_output(int32_t total_q, const uint16_t* o_lat, const uint16_t* w_kvb, const uint16_t* w_o,
-                              uint16_t* o_mid, uint16_t* y, int32_t* status, cudaStream_t stream);
+                              uint16_t* o_mid, uint16_t* y, float* part, int32_t* status, cudaStream_t stream);
+// Bytes of split-K partials dsa_mla_output needs for total_q rows (0: none).
+size_t mla_partial_bytes(int32_t total_q);
 
 }  // namespace dsa

@@ -57,10 +57,19 @@ struct GemmArgs {
     uint16_t* C;
     int64_t ldc, c_col0, c_col_step;
     int32_t tiles_m, tiles_n;
+    // split-K: splits > 1 writes fp32 partials part[s][m][ldc] (same column
+    // layout as C); reduce_kernel then sums them in split order into C
+    int32_t splits;
+    float* part;
 };
 
-__device__ __forceinline__ void tile_coords(const GemmArgs& g, int32_t tile, int32_t& b, int32_t& mt, int32_t& nt) {
+// Tile `tile` -> batch b, m-tile, n-tile and K split ks (K splits outermost).
+__device__ __forceinline__ void tile_coords(const GemmArgs& g, int32_t tile, int32_t& b, int32_t& mt, int32_t& nt,
+                                            int32_t& ks) {
     const int32_t per_batch = g.tiles_m * g.tiles_n;
+    const int32_t per_split = per_batch * g.batches;
+    ks = tile / per_split;
+    tile -= ks * per_split;
     b = tile / per_batch;
     const int32_t r = tile - b * per_batch;
     // groups of kGroupM m-tiles: within a group m moves fastest
@@ -89,8 +98,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
     const uint32_t warp = warp_id(), lane = lane_id();
 
-    const int32_t total_tiles = g.tiles_m * g.tiles_n * g.batches;
+    const int32_t total_tiles = g.tiles_m * g.tiles_n * g.batches * g.splits;
     const int32_t nk = g.K / kBK;
+    // k-tiles [k_lo(ks), k_lo(ks + 1)) belong to split ks
+    auto k_lo = [&](int32_t ks) { return (int32_t)(((int64_t)nk * ks) / g.splits); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -122,11 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int32_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                int32_t b, mt, nt;
-                tile_coords(g, tile, b, mt, nt);
+                int32_t b, mt, nt, ks;
+                tile_coords(g, tile, b, mt, nt, ks);
                 const int32_t ax = g.a_col0 + b * g.a_col_step;
                 const int32_t brow = g.b_row0 + b * g.b_row_step;
-                for (int kt = 0; kt < nk; ++kt, ++it) {
+                for (int kt = k_lo(ks); kt < k_lo(ks + 1); ++kt, ++it) {
                     const int s = it % kStages;
                     if (misc[1] || !mbar_wait(empty_bar(s), ((it / kStages) & 1u) ^ 1u)) {
                         ok = false;
@@ -166,7 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(a * kBN);
-                for (int kt = 0; kt < nk; ++kt, ++it) {
+                int32_t b, mt, nt, ks;
+                tile_coords(g, tile, b, mt, nt, ks);
+                const int32_t kt0 = k_lo(ks);
+                for (int kt = kt0; kt < k_lo(ks + 1); ++kt, ++it) {
                     const int s = it % kStages;
                     if (misc[1] || !mbar_wait(full_bar(s), (it / kStages) & 1u)) {
                         ok = false;
@@ -174,11 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int ks = 0; ks < kBK / 16; ++ks) {
-                        const uint64_t ad = sdesc_sw128(sA + s * kABytes + ks * 32, 16, 1024);
-                        const uint64_t bd = kBMn ? sdesc_sw128(sB + s * kBBytes + ks * 2048, kBBoxMnBytes, 1024)
-                                                 : sdesc_sw128(sB + s * kBBytes + ks * 32, 16, 1024);
-                        mma_bf16_ss(d, ad, bd, idesc, (kt | ks) != 0);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t ad = sdesc_sw128(sA + s * kABytes + kk * 32, 16, 1024);
+                        const uint64_t bd = kBMn ? sdesc_sw128(sB + s * kBBytes + kk * 2048, kBBoxMnBytes, 1024)
+                                                 : sdesc_sw128(sB + s * kBBytes + kk * 32, 16, 1024);
+                        mma_bf16_ss(d, ad, bd, idesc, kt != kt0 || kk != 0);
                     }
                     mma_commit(empty_bar(s));
                 }
@@ -208,17 +222,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            int32_t b, mt, nt;
-            tile_coords(g, tile, b, mt, nt);
+            int32_t b, mt, nt, ks;
+            tile_coords(g, tile, b, mt, nt, ks);
             const int32_t m = mt * kBM + row;
-            uint16_t* crow = g.C + (int64_t)m * g.ldc + g.c_col0 + (int64_t)b * g.c_col_step + (int64_t)nt * kBN;
+            const int64_t col = g.c_col0 + (int64_t)b * g.c_col_step + (int64_t)nt * kBN;
+            uint16_t* crow = g.C + (int64_t)m * g.ldc + col;
+            float* prow = g.part + ((int64_t)ks * g.M + m) * g.ldc + col;
             const uint32_t taddr = tmem_base + ((lq * 32u) << 16) + (uint32_t)(a * kBN);
 #pragma unroll 1
             for (int c = 0; c < kBN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                 tmem_ld_wait();
-                if (m < g.M && nt * kBN + c * 32 < g.N) {
+                if (m < g.M && nt * kBN + c * 32 < g.N && g.splits > 1) {
+                    float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                } else if (m < g.M && nt * kBN + c * 32 < g.N) {
                     uint4* dst = reinterpret_cast<uint4*>(crow + c * 32);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -244,6 +266,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// C[m, c] = bf16(sum over splits s, in order, of part[s][m][c]) for the
+// whole [M, ldc] footprint; 8 columns per thread.
+__global__ void reduce_kernel(int64_t M, int64_t ldc, int splits, const float* __restrict__ part,
+                              uint16_t* __restrict__ C) {
+    const int64_t n8 = M * ldc / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        float acc[8];
+        const float4* p0 = reinterpret_cast<const float4*>(part) + 2 * i;
+        float4 a = p0[0], b = p0[1];
+        acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+        acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+        for (int s = 1; s < splits; ++s) {
+            const float4* ps = reinterpret_cast<const float4*>(part + (int64_t)s * M * ldc) + 2 * i;
+            a = ps[0];
+            b = ps[1];
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+        uint4 pk;
+        pk.x = pack_bf16x2(acc[0], acc[1]);
+        pk.y = pack_bf16x2(acc[2], acc[3]);
+        pk.z = pack_bf16x2(acc[4], acc[5]);
+        pk.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4*>(C)[i] = pk;
+    }
+}
+
 // q_out[t, h, 512 + d] = q_pe[t, h, d]: one 16-byte piece per thread.
 __global__ void copy_rope_kernel(int64_t rows, const uint4* __restrict__ q_pe, uint16_t* __restrict__ q_out) {
     const int64_t n = rows * (kDRope * 2 / 16);
@@ -253,12 +302,22 @@ __global__ void copy_rope_kernel(int64_t rows, const uint4* __restrict__ q_pe, u
     }
 }
 
+// K splits of a GEMM whose output tiles fill few SMs: enough CTAs for about
+// one wave, each with at least 4 k-tiles.  Depends only on the shape.
+int choose_k_splits(int32_t M, int32_t N, int32_t K, int32_t batches) {
+    const int64_t tiles = (int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN) * batches;
+    const int32_t nk = K / kBK;
+    if (tiles == 0 || tiles * 2 > kNumSMs) return 1;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(nk / 4, kNumSMs / tiles));
+}
+
 template <bool kBMn>
 cudaError_t launch_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b, GemmArgs g, int32_t* status,
                         cudaStream_t stream) {
     g.tiles_m = (g.M + kBM - 1) / kBM;
     g.tiles_n = (g.N + kBN - 1) / kBN;
-    const int64_t tiles = (int64_t)g.tiles_m * g.tiles_n * g.batches;
+    if (g.splits < 1) g.splits = 1;
+    const int64_t tiles = (int64_t)g.tiles_m * g.tiles_n * g.batches * g.splits;
     if (tiles == 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<kBMn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
@@ -266,13 +325,27 @@ cudaError_t launch_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b, GemmAr
     const int grid = (int)std::min<int64_t>(tiles, kNumSMs);
     gemm_bf16_kernel<kBMn><<<grid, kThreads, kSmemBytes, stream>>>(tm_a, tm_b, g, status);
     e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    if (g.splits == 1) return cudaSuccess;
+    const int64_t n8 = (int64_t)g.M * g.ldc / 8;
+    const int blocks = (int)std::min<int64_t>((n8 + 255) / 256, 8 * kNumSMs);
+    reduce_kernel<<<blocks, 256, 0, stream>>>(g.M, g.ldc, g.splits, g.part, g.C);
+    e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
 
 }  // namespace
 
-size_t mla_smem_bytes() { return kSmemBytes; }
+// Split-K partials of dsa_mla_output for total_q rows (the W_UV and o_proj
+// products run one after the other and share the buffer).
+size_t mla_partial_bytes(int32_t total_q) {
+    const size_t uv = (size_t)choose_k_splits(total_q, kDVh, kDV, kH) * total_q * kH * kDVh;
+    const size_t op = (size_t)choose_k_splits(total_q, kHidden, kH * kDVh, 1) * total_q * kHidden;
+    const size_t a = std::max(uv > (size_t)total_q * kH * kDVh ? uv : 0, op > (size_t)total_q * kHidden ? op : 0);
+    return a * sizeof(float);
+}
 
 cudaError_t launch_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const uint16_t* q_pe,
                                 const uint16_t* w_kvb, uint16_t* q_out, int32_t* status, cudaStream_t stream) {
@@ -294,6 +367,8 @@ cudaError_t launch_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const u
     g.ldc = (int64_t)kH * kDQK;
     g.c_col0 = 0;
     g.c_col_step = kDQK;
+    g.splits = 1;                 // the rope columns of q_out are not the GEMM's: no split-K
+
     cudaError_t e = launch_gemm<true>(tm_a, tm_b, g, status, stream);
     if (e != cudaSuccess) return e;
     const int64_t pieces = (int64_t)total_q * kH * 8;
@@ -305,7 +380,7 @@ cudaError_t launch_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const u
 }
 
 cudaError_t launch_mla_output(int32_t total_q, const uint16_t* o_lat, const uint16_t* w_kvb, const uint16_t* w_o,
-                              uint16_t* o_mid, uint16_t* y, int32_t* status, cudaStream_t stream) {
+                              uint16_t* o_mid, uint16_t* y, float* part, int32_t* status, cudaStream_t stream) {
     if (total_q <= 0) return cudaSuccess;
     CUtensorMap tm_a, tm_b;
     // o_mid[:, h, :] = o_lat[:, h, :] . W_UV[h]^T
@@ -325,6 +400,8 @@ cudaError_t launch_mla_output(int32_t total_q, const uint16_t* o_lat, const uint
     g.ldc = (int64_t)kH * kDVh;
     g.c_col0 = 0;
     g.c_col_step = kDVh;
+    g.splits = choose_k_splits(g.M, g.N, g.K, g.batches);    // partials cover all of o_mid
+    g.part = part;
     cudaError_t e = launch_gemm<false>(tm_a, tm_b, g, status, stream);
     if (e != cudaSuccess) return e;
     // y = o_mid . W_o^T
@@ -338,6 +415,8 @@ cudaError_t launch_mla_output(int32_t total_q, const uint16_t* o_lat, const uint
     g2.batches = 1;
     g2.C = y;
     g2.ldc = kHidden;
+    g2.splits = choose_k_splits(g2.M, g2.N, g2.K, 1);
+    g2.part = part;
     return launch_gemm<false>(tm_a, tm_b, g2, status, stream);
 }
 

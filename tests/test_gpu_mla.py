@@ -35,9 +35,8 @@ def weights():
     return wn, bf16_dev(wn.w_kvb), bf16_dev(wn.w_o)
 
 
-def _ws():
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    return ws
+def _ws(T):
+    return dsa.mla_workspace(T)
 
 
 def _bits(t):
@@ -58,7 +57,7 @@ def test_absorb_q(weights, T):
     wn, w_kvb, _ = weights
     qn, qp = W.make_mla_queries_np(T, 100 + T)
     q_out = torch.full((T, 64, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = _ws()
+    ws = _ws(T)
     dsa.mla_absorb_q(bf16_dev(qn), bf16_dev(qp), w_kvb, q_out, ws)
     assert dsa.read_device_status(ws) == 0
     ref = oracle.mla_absorb_q(qn, qp, wn.w_kvb)
@@ -67,14 +66,14 @@ def test_absorb_q(weights, T):
     assert np.array_equal(_bits(q_out)[:, :, 512:], qp)          # the rope part is copied bit for bit
 
 
-@pytest.mark.parametrize("T", [1, 64, 300])
+@pytest.mark.parametrize("T", [1, 64, 300, 700])
 def test_output(weights, T):
     wn, w_kvb, w_o = weights
     rng = np.random.default_rng(200 + T)
     o_lat = W.bf16_bits_from_f32(rng.standard_normal((T, 64, 512), dtype=np.float32) * 0.3)
     o_mid = torch.full((T, 64 * 256), float("nan"), dtype=torch.bfloat16, device="cuda")
     y = torch.full((T, 6144), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = _ws()
+    ws = _ws(T)
     dsa.mla_output(bf16_dev(o_lat), w_kvb, w_o, o_mid, y, ws)
     assert dsa.read_device_status(ws) == 0
     ref_mid, ref_y = oracle.mla_output(W.f32_from_bf16_bits(o_lat).astype(np.float64), wn.w_kvb, wn.w_o)
@@ -95,7 +94,7 @@ def test_layer_against_the_expanded_path(weights):
     qn, qp = W.make_mla_queries_np(bt.total_q, 302)
     st = Staged(bt)
     T = bt.total_q
-    ws = _ws()
+    ws = _ws(T)
     q = torch.empty((T, 64, 576), dtype=torch.bfloat16, device="cuda")
     dsa.mla_absorb_q(bf16_dev(qn), bf16_dev(qp), w_kvb, q, ws)
     st.q = q
@@ -117,7 +116,7 @@ def test_projections_full_size(weights, T):
     wn, w_kvb, w_o = weights
     qn_t, qp_t = W.make_mla_queries_torch(T, 400 + T)
     q_out = torch.empty((T, 64, 576), dtype=torch.bfloat16, device="cuda")
-    ws = _ws()
+    ws = _ws(T)
     dsa.mla_absorb_q(qn_t, qp_t, w_kvb, q_out, ws)
     g = torch.Generator(device="cuda")
     g.manual_seed(500 + T)

@@ -96,9 +96,14 @@ def test_compute_entry_points_reject_bad_host_arguments(lib):
     assert lib.dsa_mla_absorb_q(4, None, p, p, p, ws, 256, None) == 1
     assert lib.dsa_mla_absorb_q(4, p, bad, p, p, ws, 256, None) == 1
     assert lib.dsa_mla_absorb_q(0, None, None, None, None, ws, 256, None) == 0
-    assert lib.dsa_mla_output(1 << 26, p, p, p, p, p, ws, 256, None) == 1
-    assert lib.dsa_mla_output(4, p, p, p, p, None, ws, 256, None) == 1
+    m = ctypes.c_size_t(0)
+    assert lib.dsa_mla_workspace_size(4, ctypes.byref(m)) == 0
+    assert lib.dsa_mla_output(1 << 26, p, p, p, p, p, ws, m.value, None) == 1
+    assert lib.dsa_mla_output(4, p, p, p, p, None, ws, m.value, None) == 1
     assert lib.dsa_mla_output(4, p, p, p, p, p, ws, 100, None) == 3
+    assert lib.dsa_mla_workspace_size(64, ctypes.byref(m)) == 0 and m.value > 64 * 6144 * 4   # split-K partials
+    assert lib.dsa_mla_output(64, p, p, p, p, p, ws, m.value - 256, None) == 3
+    assert lib.dsa_mla_workspace_size(-1, ctypes.byref(m)) == 1
     # status word helpers check their pointers on the host
     assert lib.dsa_read_device_status(None, None, None) == 1
     assert lib.dsa_reset_device_status(None, None) == 3
