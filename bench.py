@@ -39,13 +39,20 @@ import workloads as W  # noqa: E402
 DEFAULT_WORKLOAD = "decode_B64_ctx32768"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# algorithmic work per unit (see the measurement section of the design doc)
+# algorithmic work per unit
 IDX_FLOP_PER_PAIR = 2 * 32 * 128            # 8192
 IDX_BYTES_PER_KEY = 128 * 2                 # one bf16 index key
 IDX_BYTES_PER_QUERY = 32 * 128 * 2 + 32 * 4  # q_idx + w
 ATT_FLOP_PER_SEL = 2 * 64 * 576 + 2 * 64 * 512   # 139264
 ATT_BYTES_PER_SEL = 576 * 2                 # one gathered latent row
 ATT_BYTES_PER_QUERY = 64 * 576 * 2 + 64 * 512 * 2  # q in + out
+# MLA projections around the path, per token (and the weights, once per call)
+ABS_FLOP_PER_TOKEN = 2 * 64 * 192 * 512
+ABS_BYTES_PER_TOKEN = 64 * 192 * 2 + 64 * 64 * 2 + 64 * 576 * 2
+ABS_WEIGHT_BYTES = 64 * 192 * 512 * 2
+OUT_FLOP_PER_TOKEN = 2 * 64 * 512 * 256 + 2 * 64 * 256 * 6144
+OUT_BYTES_PER_TOKEN = 64 * 512 * 2 + 6144 * 2
+OUT_WEIGHT_BYTES = (64 * 256 * 512 + 6144 * 64 * 256) * 2
 
 
 def parse_args():
@@ -62,7 +69,7 @@ def parse_args():
 
 
 def default_steps(wl: W.Workload):
-    return (300, 10) if wl.kind in ("decode", "indexshare") else (20, 3)
+    return (300, 10) if wl.base in ("decode", "indexshare") else (20, 3)
 
 
 def load_peaks():
@@ -77,19 +84,24 @@ def load_peaks():
 # --------------------------------------------------------------- workloads --
 
 def metric_for(wl: W.Workload):
-    if wl.kind == "indexshare":
+    if wl.mla:
+        what = "absorbed query, indexer, top-k, attention, W_UV, o_proj"
+        if wl.base == "decode":
+            return f"MLA layer decode steps/s ({wl.B} seqs x {wl.ctx} ctx, top-{wl.k}; {what})", "steps/s"
+        return f"MLA layer prefill tokens/s (T={wl.ctx}, top-{wl.k}; {what})", "tokens/s"
+    if wl.base == "indexshare":
         return (f"IndexShare decode window steps/s ({wl.B} seqs x {wl.ctx} ctx, 1 full + {wl.steps - 1} shared "
                 f"layers, top-{wl.k})", "steps/s")
-    if wl.kind == "decode":
+    if wl.base == "decode":
         return f"decode steps/s ({wl.B} seqs x {wl.ctx} ctx, top-{wl.k}; % of HBM roofline)", "steps/s"
-    if wl.kind == "prefill":
+    if wl.base == "prefill":
         return f"prefill tokens/s (T={wl.ctx}, top-{wl.k}; % of bf16 tensor roofline)", "tokens/s"
     return f"chunked prefill tokens/s (T={wl.ctx} in {wl.ctx // wl.n_new} chunks, top-{wl.k})", "tokens/s"
 
 
 def base_config(wl: W.Workload, world: int):
     return {"workload": wl.name, "batch": wl.B, "ctx": wl.ctx, "queries_per_seq": wl.n_new, "topk": wl.k,
-            "l2": "no flush: inputs larger than L2" if wl.kind in ("decode", "indexshare") else
+            "l2": "no flush: inputs larger than L2" if wl.base in ("decode", "indexshare") else
             "no flush: the one sequence's keys and latent cache are L2-resident by design",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -103,7 +115,7 @@ class Case:
         import sparse_attention_gb300 as dsa
         self.wl, self.dev = wl, device
         self.calls = []          # (batch, slices) per dsa_forward call of one step
-        if wl.kind == "decode":
+        if wl.base == "decode":
             self.bt = W.make_batch_torch([wl.ctx] * wl.B, [1] * wl.B, wl.k, seed, key_kind=wl.key_kind,
                                          device=device, name=wl.name)
             bt = self.bt
@@ -113,7 +125,7 @@ class Case:
             self.batches = [dsa.Batch(bt.q_off, c, 1, wl.ctx, bt.stride, total_q=wl.B) for c in self.ctx_variants]
             self.positions = [[wl.ctx - wl.steps + j] * wl.B for j in range(wl.steps)]
             self.units_per_step = 1            # one decode step of the whole batch
-        elif wl.kind == "indexshare":
+        elif wl.base == "indexshare":
             # layer 0 is full; layers 1.. reuse its indices with their own q and latent cache
             self.bt = W.make_batch_torch([wl.ctx] * wl.B, [1] * wl.B, wl.k, seed, key_kind=wl.key_kind,
                                          device=device, name=wl.name)
@@ -128,7 +140,7 @@ class Case:
             self.positions = [[wl.ctx - 1] * wl.B]
             self.units_per_step = 1            # one decode step of the whole window
             self.share_idx = torch.empty((wl.B, wl.k), dtype=torch.int32, device=device)
-        elif wl.kind == "prefill":
+        elif wl.base == "prefill":
             self.bt = W.make_batch_torch([wl.ctx], [wl.n_new], wl.k, seed, key_kind=wl.key_kind, device=device,
                                          name=wl.name)
             bt = self.bt
@@ -148,6 +160,14 @@ class Case:
             self.units_per_step = T
         self.metric, self.unit = metric_for(wl)
         self.max_rows = max(b.total_q for b in self.batches)
+        if wl.mla:
+            # un-absorbed queries and random-init kv_b_proj / o_proj weights
+            T = self.max_rows
+            self.mw = W.make_mla_weights_torch(seed + 1, device=device)
+            self.q_nope, self.q_pe = W.make_mla_queries_torch(T, seed + 2, device=device)
+            self.o_mid = torch.empty((T, 64 * 256), dtype=torch.bfloat16, device=device)
+            self.y = torch.empty((T, 6144), dtype=torch.bfloat16, device=device)
+            self.mla_ws = dsa.mla_workspace(T, device=device)
         self.out = torch.empty((self.max_rows, 64, 512), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((self.max_rows, 64), dtype=torch.float32, device=device)
         self.ws = [dsa.workspace(b, wl.k, device=device) for b in self.batches]
@@ -156,7 +176,7 @@ class Case:
     def _slices(self, j):
         """query-side tensors of call j (chunked prefill slices the queries)."""
         bt, wl = self.bt, self.wl
-        if self.wl.kind == "chunked_prefill":
+        if self.wl.base == "chunked_prefill":
             C = wl.n_new
             s = slice(C * j, C * (j + 1))
             return bt.q_idx[s], bt.w[s], bt.q[s]
@@ -165,7 +185,7 @@ class Case:
     def step(self, i=0):
         """One step of the workload: every dsa_forward call it needs."""
         wl = self.wl
-        if wl.kind == "indexshare":
+        if wl.base == "indexshare":
             b = self.batches[0]
             self.dsa.forward(b, self.bt.q_idx, self.bt.w, self.bt.k_idx, self.bt.q, self.bt.kv, wl.k,
                              self.bt.sm_scale, self.out, self.lse, idx_out=self.share_idx, ws=self.ws[0])
@@ -173,21 +193,25 @@ class Case:
                 self.dsa.sparse_mla_fwd(b, q, kv, self.share_idx, wl.k, self.bt.sm_scale, self.out, self.lse,
                                         ws=self.ws[0])
             return
-        if wl.kind == "decode":
+        if wl.base == "decode":
             j = i % len(self.batches)
             calls = [j]
         else:
             calls = range(len(self.batches))
+        if wl.mla:
+            self.dsa.mla_absorb_q(self.q_nope, self.q_pe, self.mw.w_kvb, self.bt.q, self.mla_ws)
         for j in calls:
             q_idx, w, q = self._slices(j)
             b = self.batches[j]
             self.dsa.forward(b, q_idx, w, self.bt.k_idx, q, self.bt.kv, wl.k, self.bt.sm_scale,
                              self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j])
+        if wl.mla:
+            self.dsa.mla_output(self.out, self.mw.w_kvb, self.mw.w_o, self.o_mid, self.y, self.mla_ws)
 
     # algorithmic work of one step
     def work(self):
         wl = self.wl
-        calls = [0] if wl.kind in ("decode", "indexshare") else range(len(self.batches))
+        calls = [0] if wl.base in ("decode", "indexshare") else range(len(self.batches))
         idx_flop = idx_bytes = att_flop = att_bytes = topk_bytes = 0
         for j in calls:
             pos = self.positions[j]
@@ -197,15 +221,20 @@ class Case:
             att_flop += ATT_FLOP_PER_SEL * sel
             att_bytes += ATT_BYTES_PER_SEL * sel + ATT_BYTES_PER_QUERY * len(pos)
             topk_bytes += 4 * pairs + 4 * wl.k * len(pos)
-            if wl.kind == "indexshare":   # the shared layers repeat the attention only
+            if wl.base == "indexshare":   # the shared layers repeat the attention only
                 att_flop *= wl.steps
                 att_bytes *= wl.steps
-            if wl.kind in ("decode", "indexshare"):
+            if wl.base in ("decode", "indexshare"):
                 idx_bytes += IDX_BYTES_PER_KEY * sum(t + 1 for t in pos) + IDX_BYTES_PER_QUERY * len(pos)
             else:   # one sequence: keys read once per call (they stay in L2 across query groups)
                 idx_bytes += IDX_BYTES_PER_KEY * (max(pos) + 1) + IDX_BYTES_PER_QUERY * len(pos)
+        mla_flop = mla_bytes = 0
+        if wl.mla:
+            T = self.max_rows
+            mla_flop = (ABS_FLOP_PER_TOKEN + OUT_FLOP_PER_TOKEN) * T
+            mla_bytes = (ABS_BYTES_PER_TOKEN + OUT_BYTES_PER_TOKEN) * T + ABS_WEIGHT_BYTES + OUT_WEIGHT_BYTES
         return dict(idx_flop=idx_flop, idx_bytes=idx_bytes, att_flop=att_flop, att_bytes=att_bytes,
-                    topk_bytes=topk_bytes)
+                    topk_bytes=topk_bytes, mla_flop=mla_flop, mla_bytes=mla_bytes)
 
     def kernel_times_us(self, reps: int):
         """Average device time of each step call (indexer, top-k, attention):
@@ -226,6 +255,11 @@ class Case:
             "sparse_mla": lambda: dsa.sparse_mla_fwd(b, q, self.bt.kv, idx, wl.k, self.bt.sm_scale,
                                                      self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j]),
         }
+        if wl.mla:
+            calls["mla_absorb"] = lambda: dsa.mla_absorb_q(self.q_nope, self.q_pe, self.mw.w_kvb, self.bt.q,
+                                                           self.mla_ws)
+            calls["mla_output"] = lambda: dsa.mla_output(self.out, self.mw.w_kvb, self.mw.w_o, self.o_mid, self.y,
+                                                         self.mla_ws)
         times = {}
         for name, fn in calls.items():
             fn()
@@ -245,16 +279,21 @@ class Case:
         pos = self.positions[0]
         pairs = sum(t + 1 for t in pos)
         sel = sum(min(wl.k, t + 1) for t in pos)
-        if wl.kind in ("decode", "indexshare"):
+        if wl.base in ("decode", "indexshare"):
             ib = IDX_BYTES_PER_KEY * pairs + IDX_BYTES_PER_QUERY * len(pos)
         else:
             ib = IDX_BYTES_PER_KEY * (max(pos) + 1) + IDX_BYTES_PER_QUERY * len(pos)
-        return {
+        work = {
             "indexer": dict(flop=IDX_FLOP_PER_PAIR * pairs, bytes=ib),
             "topk": dict(flop=0, bytes=4 * pairs + 4 * wl.k * len(pos)),
             "sparse_mla": dict(flop=ATT_FLOP_PER_SEL * sel,
                                bytes=ATT_BYTES_PER_SEL * sel + ATT_BYTES_PER_QUERY * len(pos)),
         }
+        if wl.mla:
+            T = self.max_rows
+            work["mla_absorb"] = dict(flop=ABS_FLOP_PER_TOKEN * T, bytes=ABS_BYTES_PER_TOKEN * T + ABS_WEIGHT_BYTES)
+            work["mla_output"] = dict(flop=OUT_FLOP_PER_TOKEN * T, bytes=OUT_BYTES_PER_TOKEN * T + OUT_WEIGHT_BYTES)
+        return work
 
 
 # ------------------------------------------------------------------ clocks --
@@ -321,7 +360,7 @@ def host_sample(case: Case, n_seq: int):
     def bits(t):
         return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
-    if wl.kind == "decode":
+    if wl.base == "decode":
         ctx = wl.ctx
         n_seq = min(n_seq, wl.B)
         rows = slice(0, n_seq)
@@ -339,23 +378,39 @@ def host_sample(case: Case, n_seq: int):
     return b, rows, len(rows), f"{len(rows)} evenly spaced query rows of the {T}-token prefill"
 
 
-def oracle_path_seconds(b, rows, attention_layers: int = 1):
+def oracle_path_seconds(b, rows, attention_layers: int = 1, mla=None):
     """The oracle's whole path on `rows`; attention_layers > 1 repeats the
-    attention on the same indices (IndexShare's shared layers)."""
+    attention on the same indices (IndexShare's shared layers); mla =
+    (q_nope, q_pe, w_kv_b, w_o) of those rows adds the projections around it."""
     import oracle
     t0 = time.perf_counter()
+    if mla is not None:
+        oracle.mla_absorb_q(mla[0], mla[1], mla[2])
     sc = oracle.indexer_scores(b, rows)
     ix = oracle.topk(b, np.nan_to_num(sc.astype(np.float32), nan=0.0), rows=rows, k=b.k)
     for _ in range(attention_layers):
-        oracle.sparse_mla(b, ix, rows=rows)
+        o, _ = oracle.sparse_mla(b, ix, rows=rows)
+    if mla is not None:
+        oracle.mla_output(o, mla[2], mla[3])
     return time.perf_counter() - t0
+
+
+def _bits(t):
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
 def cpu_baseline(case: Case, unit: str):
     import oracle
-    n = 24 if case.wl.kind == "decode" else 48
+    n = 24 if case.wl.base == "decode" else 48
     b, rows, units, sample = host_sample(case, n)
-    secs = oracle_path_seconds(b, rows)
+    mla = None
+    if case.wl.mla:
+        import torch
+        ri = torch.tensor(rows, dtype=torch.long, device=case.q_nope.device)
+        mla = (_bits(case.q_nope[ri]), _bits(case.q_pe[ri]), _bits(case.mw.w_kvb), _bits(case.mw.w_o))
+        sample += "; with the MLA projections"
+    secs = oracle_path_seconds(b, rows, mla=mla)
     # units: decode -> fraction of one step; prefill -> query rows (tokens)
     return {"value": units / secs, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": sample + f" (full path: indexer, top-k, attention; {secs:.1f} s in fp64)"}
@@ -374,8 +429,8 @@ def run_reference(args):
     K = args.steps if args.steps is not None else K
     Wu = args.warmup if args.warmup is not None else Wu
     # one bounded sample per step, drawn with the numpy recipe
-    shared_layers = wl.steps - 1 if wl.kind == "indexshare" else 0
-    if wl.kind in ("decode", "indexshare"):
+    shared_layers = wl.steps - 1 if wl.base == "indexshare" else 0
+    if wl.base in ("decode", "indexshare"):
         ns = 1
         b = W.make_batch_np([wl.ctx] * ns, [1] * ns, wl.k, wl.seed, key_kind=wl.key_kind)
         rows = list(range(ns))
@@ -391,8 +446,15 @@ def run_reference(args):
         rows = [int(x) for x in np.linspace(0, T - 1, nq)]
         frac = nq
         sample = f"{nq} evenly spaced query rows per timed step"
+    mla = None
+    if wl.mla:
+        mw = W.make_mla_weights_np(wl.seed + 1)
+        qn, qp = W.make_mla_queries_np(len(rows), wl.seed + 2)
+        mla = (qn, qp, mw.w_kvb, mw.w_o)
+        sample += "; with the MLA projections"
+
     def one_step():
-        oracle_path_seconds(b, rows, 1 + shared_layers)
+        oracle_path_seconds(b, rows, 1 + shared_layers, mla=mla)
 
     for _ in range(Wu):
         one_step()
@@ -504,7 +566,7 @@ def run_dsa(args):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e and wl.kind != "indexshare":
+    if not args.no_e2e and wl.base != "indexshare":
         e2e = run_e2e(case, K, Wu, barrier, lambda x: max_over_ranks(x, dev), world)
 
     # per-kernel device times and the roofline of the dominant kernel
@@ -514,7 +576,7 @@ def run_dsa(args):
     peaks, peak_src = load_peaks()
     dom = max(times, key=times.get)
     kw = work[dom]
-    if wl.kind not in ("decode", "indexshare") and dom in ("indexer", "sparse_mla"):
+    if wl.base not in ("decode", "indexshare") and dom in ("indexer", "sparse_mla", "mla_absorb", "mla_output"):
         achieved = kw["flop"] / (times[dom] * 1e-6) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"]}
@@ -530,7 +592,7 @@ def run_dsa(args):
     if rank != 0:
         return
     cpu = None
-    if not args.no_cpu_baseline and world == 1 and wl.kind != "indexshare":
+    if not args.no_cpu_baseline and world == 1 and wl.base != "indexshare":
         cpu = cpu_baseline(case, case.unit)
     wk = case.work()
     cfg = base_config(wl, world)
@@ -538,7 +600,11 @@ def run_dsa(args):
                                         "attention_tflop": wk["att_flop"] / 1e12,
                                         "indexer_gb": wk["idx_bytes"] / 1e9, "attention_gb": wk["att_bytes"] / 1e9},
                "device_status": status}
-    if wl.kind in ("decode", "indexshare"):
+    if wl.mla:
+        details["algorithmic_per_step"].update({"mla_projection_tflop": wk["mla_flop"] / 1e12,
+                                                "mla_projection_gb": wk["mla_bytes"] / 1e9})
+        details["mla_device_status"] = dsa.read_device_status(case.mla_ws)
+    if wl.base in ("decode", "indexshare"):
         details["tokens_per_s"] = value * wl.B
     line = {"metric": case.metric, "value": value, "unit": case.unit, "n_gpus": world, "steps": K, "warmup": Wu,
             "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -555,36 +621,45 @@ def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
     import torch
     wl, bt = case.wl, case.bt
     stream = torch.cuda.current_stream()
-    if wl.kind == "decode":
-        host = {"q_idx": bt.q_idx.cpu().pin_memory(), "w": bt.w.cpu().pin_memory(), "q": bt.q.cpu().pin_memory()}
+    # the step's query-side inputs and result: the absorbed q and the latent
+    # output, or (MLA layer) q_nope / q_pe and the o_proj output y
+    if wl.mla:
+        qside = {"q_nope": case.q_nope, "q_pe": case.q_pe}
+        result = case.y
+    else:
+        qside = {"q": bt.q}
+        result = case.out
+    if wl.base == "decode":
+        host = {"q_idx": bt.q_idx.cpu().pin_memory(), "w": bt.w.cpu().pin_memory()}
+        host.update({k: v.cpu().pin_memory() for k, v in qside.items()})
         kv3 = bt.kv.view(wl.B, bt.stride, 576)
         ki3 = bt.k_idx.view(wl.B, bt.stride, 128)
         new_kv = kv3[:, wl.ctx - 1].cpu().pin_memory()
         new_ki = ki3[:, wl.ctx - 1].cpu().pin_memory()
-        out_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+        out_h = torch.empty(result.shape, dtype=result.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + [new_kv, new_ki])
         d2h = out_h.numel() * out_h.element_size()
+        dev_of = {"q_idx": bt.q_idx, "w": bt.w, **qside}
 
         def step(i):
-            bt.q_idx.copy_(host["q_idx"], non_blocking=True)
-            bt.w.copy_(host["w"], non_blocking=True)
-            bt.q.copy_(host["q"], non_blocking=True)
+            for name, t in host.items():
+                dev_of[name].copy_(t, non_blocking=True)
             kv3[:, wl.ctx - 1].copy_(new_kv, non_blocking=True)
             ki3[:, wl.ctx - 1].copy_(new_ki, non_blocking=True)
             case.step(len(case.batches) - 1)
-            out_h.copy_(case.out, non_blocking=True)
+            out_h.copy_(result, non_blocking=True)
     else:
-        host = {"q_idx": bt.q_idx.cpu().pin_memory(), "w": bt.w.cpu().pin_memory(), "q": bt.q.cpu().pin_memory(),
-                "kv": bt.kv.cpu().pin_memory(), "k_idx": bt.k_idx.cpu().pin_memory()}
-        out_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+        dev_of = {"q_idx": bt.q_idx, "w": bt.w, "kv": bt.kv, "k_idx": bt.k_idx, **qside}
+        host = {k: v.cpu().pin_memory() for k, v in dev_of.items()}
+        out_h = torch.empty(result.shape, dtype=result.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_h.numel() * out_h.element_size()
 
         def step(i):
             for name, t in host.items():
-                getattr(bt, name).copy_(t, non_blocking=True)
+                dev_of[name].copy_(t, non_blocking=True)
             case.step(i)
-            out_h.copy_(case.out, non_blocking=True)
+            out_h.copy_(result, non_blocking=True)
     for i in range(Wu):
         step(i)
     barrier()
@@ -596,8 +671,9 @@ def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1))
     value = whole_job_value(case.units_per_step, K, world, ms)
-    return {"value": value, "unit": case.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "api": "sparse_attention_gb300.forward"}
+    api = ("sparse_attention_gb300.mla_absorb_q + forward + mla_output" if wl.mla
+           else "sparse_attention_gb300.forward")
+    return {"value": value, "unit": case.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": api}
 
 
 def main():

@@ -221,6 +221,16 @@ class Workload:
     seed: int
     steps: int = 1              # decode steps (long decode) or chunks (chunked prefill)
 
+    @property
+    def mla(self) -> bool:
+        """The MLA projections around the path are part of the step."""
+        return self.kind.startswith("mla_")
+
+    @property
+    def base(self) -> str:
+        """The kind of the DSA part of the step."""
+        return self.kind[4:] if self.mla else self.kind
+
     def describe(self) -> Dict[str, object]:
         return dataclasses.asdict(self)
 
@@ -239,6 +249,10 @@ WORKLOADS: Dict[str, Workload] = {
     # attention) and three shared layers reusing its indices (steps = layers)
     "indexshare_decode_B64_ctx32768_w4": Workload("indexshare_decode_B64_ctx32768_w4", "indexshare", 64, 32768, 1,
                                                   TOPK, "iid", 20265, steps=4),
+    # the decode and prefill workloads with the MLA projections around the
+    # path: absorb the query (W_UK), then W_UV and o_proj on the output
+    "mla_decode_B64_ctx32768": Workload("mla_decode_B64_ctx32768", "mla_decode", 64, 32768, 1, TOPK, "iid", 20266),
+    "mla_prefill_T16384": Workload("mla_prefill_T16384", "mla_prefill", 1, 16384, 16384, TOPK, "lowrank16", 20267),
     # long decode: 8 sequences at 202752 context, 4 decode steps
     "long_decode_B8_ctx202752": Workload("long_decode_B8_ctx202752", "decode", 8, MAX_POS, 1, TOPK, "zipf",
                                          20264, steps=4),
