@@ -13,6 +13,7 @@ Functions (all take numpy arrays; bf16 tensors as uint16 bit patterns):
   mla_absorb_q(q_nope, q_pe, w_kvb)    -> float64 [T, 64, 576]
   mla_output(o_lat, w_kvb, w_o)        -> (float64 [T, 64, 256], float64 [T, 6144])
   mla_expanded(batch, q_nope, q_pe, w_kvb, w_o, idx, rows) -> same pair, the pages' expanded path
+  index_key(x, wk, gamma, beta, eps, cos, sin, ww) -> (float64 [T, 128], float64 [T, 32])
 See ``oracle.c`` for what each computes and the passages it follows.
 """
 
@@ -66,6 +67,7 @@ def _load():
             lib.oracle_mla_absorb_q.argtypes = [i32, P, P, P, P]
             lib.oracle_mla_output.argtypes = [i32, P, P, P, P, P]
             lib.oracle_mla_expanded.argtypes = [i32, P, P, i64, P, P, P, P, P, P, i32, dbl, i32, P, P, P]
+            lib.oracle_index_key.argtypes = [i32, P, P, P, P, dbl, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -242,3 +244,27 @@ def mla_expanded(batch, q_nope, q_pe, w_kvb, w_o, idx, rows=None, sm_scale=None)
                                 _ptr(wk), _ptr(wo), _ptr(idx), idx.shape[1], scale, len(r), _ptr(r), _ptr(o_mid),
                                 _ptr(y))
     return o_mid, y
+
+
+def index_key(x, wk, gamma, beta, eps, cos, sin, ww) -> Tuple[np.ndarray, np.ndarray]:
+    """Index keys of new tokens (wk, LayerNorm(128), RoPE on the first 64
+    dims with the given cos / sin rows) and their head weights
+    (weights_proj * 32^-1/2)."""
+    xb = _np(x, np.uint16)
+    T = xb.size // HIDDEN
+    if xb.size != T * HIDDEN:
+        raise ValueError("x is not [T, 6144]")
+    wkb, wwb = _np(wk, np.uint16), _np(ww, np.uint16)
+    if wkb.size != D_IDX * HIDDEN or wwb.size != H_IDX * HIDDEN:
+        raise ValueError("wk must be [128, 6144] and weights_proj [32, 6144]")
+    g = np.ascontiguousarray(np.asarray(gamma, dtype=np.float64))
+    b = np.ascontiguousarray(np.asarray(beta, dtype=np.float64))
+    c = np.ascontiguousarray(np.asarray(cos, dtype=np.float64))
+    s = np.ascontiguousarray(np.asarray(sin, dtype=np.float64))
+    if g.size != D_IDX or b.size != D_IDX or c.size != T * 64 or s.size != T * 64:
+        raise ValueError("gamma / beta must hold 128 values, cos / sin [T, 64]")
+    k = np.empty((T, D_IDX), dtype=np.float64)
+    w = np.empty((T, H_IDX), dtype=np.float64)
+    _load().oracle_index_key(T, _ptr(xb), _ptr(wkb), _ptr(g), _ptr(b), float(eps), _ptr(c), _ptr(s), _ptr(wwb),
+                             _ptr(k), _ptr(w))
+    return k, w

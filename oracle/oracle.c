@@ -54,6 +54,17 @@
  *  oracle_mla_output      -- the absorbed output: o[h] = W_UV[h] o_lat[h]
  *      (sum p (W_UV c) = W_UV sum p c), then y = o_proj(o).
  *
+ * The index-key producer ("GLM-5.1 架构深度拆解", section 3.6 Steps 2-4):
+ *  oracle_index_key       -- for each new token with hidden state x:
+ *      k = LayerNorm(wk x) over its 128 dims (k_norm: mean, biased
+ *      variance, eps, then gamma and beta), RoPE on the first 64 dims with
+ *      the caller's cos / sin of the token's position (the rotate-half
+ *      form: pairs (i, i + 32)), the last 64 dims unchanged; and the head
+ *      weights w = (weights_proj x) * 32^-1/2.  The pages give neither the
+ *      rotary base nor the pairing; the cos / sin rows come in as inputs
+ *      (the rotary table of the position embedding) and the pairing is the
+ *      rotate-half one of the pages' apply_rotary_pos_emb.
+ *
  * Plain loops, no blocking, no reordering; OpenMP only splits query rows.
  */
 #include <math.h>
@@ -66,6 +77,7 @@
 
 enum { O_HIDX = 32, O_DIDX = 128, O_H = 64, O_DQK = 576, O_DV = 512 };
 enum { O_DNOPE = 192, O_DROPE = 64, O_DVH = 256, O_KVB = 448, O_HID = 6144 };
+enum { O_KROPE = 64 };   /* the RoPE part of an index key: its first 64 dims */
 
 static double widen_bf16(uint16_t b) {
     uint32_t u = ((uint32_t)b) << 16;
@@ -389,5 +401,42 @@ void oracle_mla_expanded(int B, const int32_t* q_off, const int32_t* ctx_len, in
         free(logit);
         free(kn);
         free(v);
+    }
+}
+
+/* k_out[t, 0:128] and w_out[t, 0:32] for T tokens. */
+void oracle_index_key(int T, const uint16_t* x, const uint16_t* wk, const double* gamma, const double* beta,
+                      double eps, const double* cos_t, const double* sin_t, const uint16_t* ww, double* k_out,
+                      double* w_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; t++) {
+        const uint16_t* xt = x + (int64_t)t * O_HID;
+        double y[O_DIDX], z[O_DIDX];
+        for (int j = 0; j < O_DIDX; j++) {
+            double acc = 0.0;
+            for (int c = 0; c < O_HID; c++) acc += widen_bf16(wk[(int64_t)j * O_HID + c]) * widen_bf16(xt[c]);
+            y[j] = acc;
+        }
+        double mean = 0.0;
+        for (int j = 0; j < O_DIDX; j++) mean += y[j];
+        mean /= O_DIDX;
+        double var = 0.0;
+        for (int j = 0; j < O_DIDX; j++) var += (y[j] - mean) * (y[j] - mean);
+        var /= O_DIDX;
+        for (int j = 0; j < O_DIDX; j++) z[j] = (y[j] - mean) / sqrt(var + eps) * gamma[j] + beta[j];
+        double* kt = k_out + (int64_t)t * O_DIDX;
+        const double* ct = cos_t + (int64_t)t * O_KROPE;
+        const double* st = sin_t + (int64_t)t * O_KROPE;
+        for (int i = 0; i < O_KROPE; i++) {
+            /* rotate_half: (-z[i + 32], z[i - 32]) */
+            double rh = i < O_KROPE / 2 ? -z[i + O_KROPE / 2] : z[i - O_KROPE / 2];
+            kt[i] = z[i] * ct[i] + rh * st[i];
+        }
+        for (int j = O_KROPE; j < O_DIDX; j++) kt[j] = z[j];
+        for (int h = 0; h < O_HIDX; h++) {
+            double acc = 0.0;
+            for (int c = 0; c < O_HID; c++) acc += widen_bf16(ww[(int64_t)h * O_HID + c]) * widen_bf16(xt[c]);
+            w_out[(int64_t)t * O_HIDX + h] = acc / sqrt((double)O_HIDX);
+        }
     }
 }

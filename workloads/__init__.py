@@ -304,3 +304,45 @@ def make_mla_queries_torch(total_q: int, seed: int, device: str = "cuda"):
     q_nope = torch.randn(total_q, H, D_NOPE, generator=g, device=device).to(torch.bfloat16)
     q_pe = torch.randn(total_q, H, D_ROPE, generator=g, device=device).to(torch.bfloat16)
     return q_nope, q_pe
+
+
+# --------------------------------------------------------------------------
+# the index-key producer: hidden states, wk / k_norm / weights_proj, rotary rows
+# --------------------------------------------------------------------------
+
+ROPE_THETA = 10000.0    # synthetic rotary base (the tables are inputs of the producer)
+
+
+@dataclasses.dataclass
+class IndexKeyParams:
+    """wk [128, 6144] and weights_proj [32, 6144] (bf16 bits / tensors),
+    k_norm gamma / beta [128] (fp32), eps."""
+    wk: object
+    ww: object
+    gamma: object
+    beta: object
+    eps: float = 1e-5
+
+
+def rotary_rows(positions, dim: int = 64, theta: float = ROPE_THETA):
+    """cos / sin rows [n, dim] of the rotate-half rotary table at the given
+    positions (frequencies repeated over the two halves), fp32 numpy."""
+    pos = np.asarray(positions, dtype=np.float64)[:, None]
+    inv = theta ** (-np.arange(0, dim, 2, dtype=np.float64) / dim)
+    ang = pos * np.concatenate([inv, inv])[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def make_index_key_params_np(seed: int) -> IndexKeyParams:
+    rng = np.random.default_rng(seed)
+    wk = rng.standard_normal((D_IDX, HIDDEN), dtype=np.float32) / math.sqrt(HIDDEN)
+    ww = rng.standard_normal((H_IDX, HIDDEN), dtype=np.float32) / math.sqrt(HIDDEN)
+    gamma = (1.0 + 0.1 * rng.standard_normal(D_IDX)).astype(np.float32)
+    beta = (0.1 * rng.standard_normal(D_IDX)).astype(np.float32)
+    return IndexKeyParams(bf16_bits_from_f32(wk), bf16_bits_from_f32(ww), gamma, beta)
+
+
+def make_hidden_np(total_q: int, seed: int) -> np.ndarray:
+    """Hidden states [total_q, 6144] ~ N(0, 1), bf16 bits."""
+    rng = np.random.default_rng(seed)
+    return bf16_bits_from_f32(rng.standard_normal((total_q, HIDDEN), dtype=np.float32))
