@@ -255,6 +255,39 @@ DSA_API dsa_status dsa_mla_output(int32_t total_q, const uint16_t* o_lat, const 
                                   const uint16_t* w_o, uint16_t* o_mid, uint16_t* y, void* ws, size_t ws_bytes,
                                   void* stream);
 
+/* ---- The index-key producer ("GLM-5.1 架构深度拆解", section 3.6 Steps 2-4):
+ * the step before the indexer, for the new tokens of a call.  For the new
+ * token at packed row r (sequence b, position t = ctx_len[b] - n_b + i):
+ *   k = LayerNorm(wk x[r])            over 128 dims: mean, biased variance,
+ *                                     (v - mean) / sqrt(var + eps) * gamma + beta
+ *   k[i] = k[i] cos[r,i] - k[i+32] sin[r,i],  k[i+32] = k[i+32] cos[r,i+32]
+ *          + k[i] sin[r,i+32]  for i < 32 (rotate-half RoPE on dims 0..63)
+ *   k_idx[b * cache_stride + t] = bf16(k)     (the cache append)
+ *   w_out[r, h] = (w_proj x[r])[h] * 32^-1/2  (the w of dsa_indexer_scores)
+ * fp32 accumulation and arithmetic; k rounded to bf16 (nearest even).  The
+ * pages fix neither the rotary base nor the pairing: the caller passes the
+ * rows of its rotary table (cos / sin of the token's position, fp32 [64]),
+ * the pairing is the rotate-half one.
+ * Layouts (row-major, DEVICE, 16-byte aligned):
+ *   x       bf16 [total_q, 6144]   hidden states of the new tokens
+ *   wk      bf16 [128, 6144]       indexer key projection (nn.Linear layout)
+ *   gamma, beta fp32 [128]         k_norm affine parameters
+ *   cos, sin fp32 [total_q, 64]    rotary rows of each token's position
+ *   w_proj  bf16 [32, 6144]        indexer weights_proj
+ *   k_idx   bf16 [batch * cache_stride, 128]   index-key cache (only the new
+ *                                  tokens' rows are written)
+ *   w_out   fp32 [total_q, 32]
+ * ws: at least dsa_index_key_workspace_size(total_q) bytes (status header
+ * plus fp32 partial sums), else DSA_ERR_WORKSPACE.  Errors: bad batch,
+ * null or misaligned pointers, eps not positive and finite ->
+ * DSA_ERR_INVALID_ARG; rows the device-side q_off / ctx_len leave
+ * inconsistent are skipped and DSA_ERR_BAD_BATCH is latched. */
+DSA_API dsa_status dsa_index_key_workspace_size(int32_t total_q, size_t* bytes);
+DSA_API dsa_status dsa_index_key_producer(const dsa_batch* batch, const uint16_t* x, const uint16_t* wk,
+                                          const float* gamma, const float* beta, float eps, const float* cos,
+                                          const float* sin, const uint16_t* w_proj, uint16_t* k_idx, float* w_out,
+                                          void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,8 @@ STATUS = {
 
 EXPORTS = ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
            "dsa_selftest_wait_timeout", "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd",
-           "dsa_sparse_mla_fwd_noalloc", "dsa_forward", "dsa_mla_absorb_q", "dsa_mla_workspace_size", "dsa_mla_output")
+           "dsa_sparse_mla_fwd_noalloc", "dsa_forward", "dsa_mla_absorb_q", "dsa_mla_workspace_size", "dsa_mla_output", "dsa_index_key_workspace_size",
+           "dsa_index_key_producer")
 
 
 class DsaError(RuntimeError):
@@ -82,6 +83,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_mla_absorb_q.argtypes = [i32, P, P, P, P, P, sz, P]
     lib.dsa_mla_output.argtypes = [i32, P, P, P, P, P, P, sz, P]
     lib.dsa_mla_workspace_size.argtypes = [i32, ctypes.POINTER(sz)]
+    lib.dsa_index_key_workspace_size.argtypes = [i32, ctypes.POINTER(sz)]
+    lib.dsa_index_key_producer.argtypes = [BP, P, P, P, P, f32, P, P, P, P, P, P, sz, P]
     for name in EXPORTS:
         if name not in ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count"):
             getattr(lib, name).restype = ctypes.c_int
@@ -264,3 +267,25 @@ def mla_output(o_lat, w_kv_b, w_o, o_mid, y, ws, stream=None):
     _check(load_library().dsa_mla_output(int(total_q), _bf16(o_lat), _bf16(w_kv_b), _bf16(w_o), _bf16(o_mid),
                                          _bf16(y), _p(ws), ws.numel(), _stream(stream)), "dsa_mla_output")
     return y
+
+
+def index_key_workspace(total_q: int, device="cuda") -> torch.Tensor:
+    n = ctypes.c_size_t(0)
+    _check(load_library().dsa_index_key_workspace_size(int(total_q), ctypes.byref(n)),
+           "dsa_index_key_workspace_size")
+    ws = torch.empty(max(int(n.value), 256), dtype=torch.uint8, device=device)
+    reset_device_status(ws)
+    return ws
+
+
+def index_key_producer(batch: Batch, x, wk, gamma, beta, eps: float, cos, sin, w_proj, k_idx, w_out, ws,
+                       stream=None):
+    """Index keys of the batch's new tokens appended to k_idx, and their head
+    weights in w_out (see dsa_index_key_producer)."""
+    for t in (gamma, beta, cos, sin, w_out):
+        assert t.dtype == torch.float32
+    _check(load_library().dsa_index_key_producer(ctypes.byref(batch.c), _bf16(x), _bf16(wk), _p(gamma), _p(beta),
+                                                 float(eps), _p(cos), _p(sin), _bf16(w_proj), _bf16(k_idx),
+                                                 _p(w_out), _p(ws), ws.numel(), _stream(stream)),
+           "dsa_index_key_producer")
+    return k_idx

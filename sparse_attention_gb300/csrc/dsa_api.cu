@@ -246,4 +246,29 @@ dsa_status dsa_mla_output(int32_t total_q, const uint16_t* o_lat, const uint16_t
                                          static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status dsa_index_key_workspace_size(int32_t total_q, size_t* bytes) {
+    if (!bytes || total_q < 0 || total_q >= (1 << 26)) return DSA_ERR_INVALID_ARG;
+    *bytes = round_up(kWsHeaderBytes + index_key_partial_bytes(total_q), 256);
+    return DSA_OK;
+}
+
+dsa_status dsa_index_key_producer(const dsa_batch* batch, const uint16_t* x, const uint16_t* wk, const float* gamma,
+                                  const float* beta, float eps, const float* cos_t, const float* sin_t,
+                                  const uint16_t* w_proj, uint16_t* k_idx, float* w_out, void* ws, size_t ws_bytes,
+                                  void* stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (!ws || !aligned16(ws) || ws_bytes < kWsHeaderBytes + index_key_partial_bytes(batch->total_q))
+        return DSA_ERR_WORKSPACE;
+    if (batch->total_q == 0) return DSA_OK;
+    if (!x || !wk || !gamma || !beta || !cos_t || !sin_t || !w_proj || !k_idx || !w_out) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(wk) || !aligned16(gamma) || !aligned16(beta) || !aligned16(cos_t) ||
+        !aligned16(sin_t) || !aligned16(w_proj) || !aligned16(k_idx) || !aligned16(w_out))
+        return DSA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || eps == INFINITY) return DSA_ERR_INVALID_ARG;
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsHeaderBytes);
+    return cuda_status(launch_index_key(to_dev(batch), x, wk, gamma, beta, eps, cos_t, sin_t, w_proj, k_idx, w_out,
+                                        part, static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -100,4 +100,19 @@ cudaError_t launch_mla_output(int32_t total_q, const uint16_t* o_lat, const uint
 // Bytes of split-K partials dsa_mla_output needs for total_q rows (0: none).
 size_t mla_partial_bytes(int32_t total_q);
 
+// C = A . B^T for a K-major A [M, K] and K-major B [N, K] (tensor maps with
+// boxes {64, 128} and {64, 256}), fp32 results part[s][m][n] of `splits`
+// equal K splits (their sum is the product); K a multiple of 64.
+cudaError_t launch_gemm_f32_parts(const CUtensorMap& tm_a, const CUtensorMap& tm_b, int32_t M, int32_t N, int32_t K,
+                                  int32_t splits, float* part, int32_t* status, cudaStream_t stream);
+// The K splits launch_gemm_f32_parts should use for an M x N x K product.
+int gemm_k_splits(int32_t M, int32_t N, int32_t K);
+
+// The index-key producer: workspace bytes past the status header, launch.
+size_t index_key_partial_bytes(int32_t total_q);
+cudaError_t launch_index_key(const BatchDev& bd, const uint16_t* x, const uint16_t* wk, const float* gamma,
+                             const float* beta, float eps, const float* cos_t, const float* sin_t,
+                             const uint16_t* w_proj, uint16_t* k_idx, float* w_out, float* part, int32_t* status,
+                             cudaStream_t stream);
+
 }  // namespace dsa

@@ -58,9 +58,11 @@ struct GemmArgs {
     int64_t ldc, c_col0, c_col_step;
     int32_t tiles_m, tiles_n;
     // split-K: splits > 1 writes fp32 partials part[s][m][ldc] (same column
-    // layout as C); reduce_kernel then sums them in split order into C
+    // layout as C); reduce_kernel then sums them in split order into C.
+    // out_fp32: the partials are the result (no bf16 C, no reduce).
     int32_t splits;
     float* part;
+    int32_t out_fp32;
 };
 
 // Tile `tile` -> batch b, m-tile, n-tile and K split ks (K splits outermost).
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), r);
                 tmem_ld_wait();
-                if (m < g.M && nt * kBN + c * 32 < g.N && g.splits > 1) {
+                if (m < g.M && nt * kBN + c * 32 < g.N && (g.splits > 1 || g.out_fp32)) {
                     float4* dst = reinterpret_cast<float4*>(prow + c * 32);
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
@@ -327,7 +329,7 @@ cudaError_t launch_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b, GemmAr
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1);
-    if (g.splits == 1) return cudaSuccess;
+    if (g.splits == 1 || g.out_fp32) return cudaSuccess;
     const int64_t n8 = (int64_t)g.M * g.ldc / 8;
     const int blocks = (int)std::min<int64_t>((n8 + 255) / 256, 8 * kNumSMs);
     reduce_kernel<<<blocks, 256, 0, stream>>>(g.M, g.ldc, g.splits, g.part, g.C);
@@ -337,6 +339,22 @@ cudaError_t launch_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b, GemmAr
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_f32_parts(const CUtensorMap& tm_a, const CUtensorMap& tm_b, int32_t M, int32_t N, int32_t K,
+                                  int32_t splits, float* part, int32_t* status, cudaStream_t stream) {
+    GemmArgs g{};
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.batches = 1;
+    g.ldc = N;
+    g.splits = splits;
+    g.part = part;
+    g.out_fp32 = 1;
+    return launch_gemm<false>(tm_a, tm_b, g, status, stream);
+}
+
+int gemm_k_splits(int32_t M, int32_t N, int32_t K) { return choose_k_splits(M, N, K, 1); }
 
 // Split-K partials of dsa_mla_output for total_q rows (the W_UV and o_proj
 // products run one after the other and share the buffer).

@@ -104,6 +104,12 @@ def test_compute_entry_points_reject_bad_host_arguments(lib):
     assert lib.dsa_mla_workspace_size(64, ctypes.byref(m)) == 0 and m.value > 64 * 6144 * 4   # split-K partials
     assert lib.dsa_mla_output(64, p, p, p, p, p, ws, m.value - 256, None) == 3
     assert lib.dsa_mla_workspace_size(-1, ctypes.byref(m)) == 1
+    # index-key producer: workspace, pointers, eps
+    assert lib.dsa_index_key_workspace_size(4, ctypes.byref(m)) == 0 and m.value >= 256
+    assert lib.dsa_index_key_producer(B, p, p, p, p, ctypes.c_float(1e-5), p, p, p, p, p, ws, 100, None) == 3
+    assert lib.dsa_index_key_producer(B, p, p, p, p, ctypes.c_float(0.0), p, p, p, p, p, ws, m.value, None) == 1
+    assert lib.dsa_index_key_producer(B, p, None, p, p, ctypes.c_float(1e-5), p, p, p, p, p, ws, m.value, None) == 1
+    assert lib.dsa_index_key_producer(B, p, p, p, bad, ctypes.c_float(1e-5), p, p, p, p, p, ws, m.value, None) == 1
     # status word helpers check their pointers on the host
     assert lib.dsa_read_device_status(None, None, None) == 1
     assert lib.dsa_reset_device_status(None, None) == 3
