@@ -53,6 +53,9 @@ ABS_WEIGHT_BYTES = 64 * 192 * 512 * 2
 OUT_FLOP_PER_TOKEN = 2 * 64 * 512 * 256 + 2 * 64 * 256 * 6144
 OUT_BYTES_PER_TOKEN = 64 * 512 * 2 + 6144 * 2
 OUT_WEIGHT_BYTES = (64 * 256 * 512 + 6144 * 64 * 256) * 2
+IK_FLOP_PER_TOKEN = 2 * 6144 * (128 + 32)                  # wk and weights_proj
+IK_BYTES_PER_TOKEN = 6144 * 2 + 128 * 2 + 32 * 4 + 64 * 8   # x in, key and w out, cos / sin rows
+IK_WEIGHT_BYTES = (128 + 32) * 6144 * 2
 
 
 def parse_args():
@@ -85,7 +88,7 @@ def load_peaks():
 
 def metric_for(wl: W.Workload):
     if wl.mla:
-        what = "absorbed query, indexer, top-k, attention, W_UV, o_proj"
+        what = "index-key producer, absorbed query, indexer, top-k, attention, W_UV, o_proj"
         if wl.base == "decode":
             return f"MLA layer decode steps/s ({wl.B} seqs x {wl.ctx} ctx, top-{wl.k}; {what})", "steps/s"
         return f"MLA layer prefill tokens/s (T={wl.ctx}, top-{wl.k}; {what})", "tokens/s"
@@ -168,6 +171,20 @@ class Case:
             self.o_mid = torch.empty((T, 64 * 256), dtype=torch.bfloat16, device=device)
             self.y = torch.empty((T, 6144), dtype=torch.bfloat16, device=device)
             self.mla_ws = dsa.mla_workspace(T, device=device)
+            # the index-key producer: hidden states, wk / k_norm / weights_proj, rotary rows
+            ip = W.make_index_key_params_np(seed + 3)
+            g = torch.Generator(device=device)
+            g.manual_seed(seed + 4)
+            self.x = torch.randn(T, W.HIDDEN, generator=g, device=device).to(torch.bfloat16)
+            self.ik = {"wk": torch.from_numpy(ip.wk.view(np.int16)).to(device).view(torch.bfloat16),
+                       "ww": torch.from_numpy(ip.ww.view(np.int16)).to(device).view(torch.bfloat16),
+                       "gamma": torch.from_numpy(ip.gamma).to(device), "beta": torch.from_numpy(ip.beta).to(device),
+                       "eps": ip.eps}
+            self.rope = []
+            for pos in self.positions:
+                c, sn = W.rotary_rows(pos)
+                self.rope.append((torch.from_numpy(c).to(device), torch.from_numpy(sn).to(device)))
+            self.ik_ws = [dsa.index_key_workspace(b.total_q, device=device) for b in self.batches]
         self.out = torch.empty((self.max_rows, 64, 512), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((self.max_rows, 64), dtype=torch.float32, device=device)
         self.ws = [dsa.workspace(b, wl.k, device=device) for b in self.batches]
@@ -199,6 +216,8 @@ class Case:
         else:
             calls = range(len(self.batches))
         if wl.mla:
+            for j in calls:
+                self._index_key(j)
             self.dsa.mla_absorb_q(self.q_nope, self.q_pe, self.mw.w_kvb, self.bt.q, self.mla_ws)
         for j in calls:
             q_idx, w, q = self._slices(j)
@@ -207,6 +226,12 @@ class Case:
                              self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j])
         if wl.mla:
             self.dsa.mla_output(self.out, self.mw.w_kvb, self.mw.w_o, self.o_mid, self.y, self.mla_ws)
+
+    def _index_key(self, j):
+        """The new tokens' index keys (appended to the cache) and head weights."""
+        b, (c, sn), ik = self.batches[j], self.rope[j], self.ik
+        self.dsa.index_key_producer(b, self.x[:b.total_q], ik["wk"], ik["gamma"], ik["beta"], ik["eps"], c, sn,
+                                    ik["ww"], self.bt.k_idx, self.bt.w[:b.total_q], self.ik_ws[j])
 
     # algorithmic work of one step
     def work(self):
@@ -231,8 +256,9 @@ class Case:
         mla_flop = mla_bytes = 0
         if wl.mla:
             T = self.max_rows
-            mla_flop = (ABS_FLOP_PER_TOKEN + OUT_FLOP_PER_TOKEN) * T
-            mla_bytes = (ABS_BYTES_PER_TOKEN + OUT_BYTES_PER_TOKEN) * T + ABS_WEIGHT_BYTES + OUT_WEIGHT_BYTES
+            mla_flop = (ABS_FLOP_PER_TOKEN + OUT_FLOP_PER_TOKEN + IK_FLOP_PER_TOKEN) * T
+            mla_bytes = ((ABS_BYTES_PER_TOKEN + OUT_BYTES_PER_TOKEN + IK_BYTES_PER_TOKEN) * T + ABS_WEIGHT_BYTES
+                         + OUT_WEIGHT_BYTES + IK_WEIGHT_BYTES)
         return dict(idx_flop=idx_flop, idx_bytes=idx_bytes, att_flop=att_flop, att_bytes=att_bytes,
                     topk_bytes=topk_bytes, mla_flop=mla_flop, mla_bytes=mla_bytes)
 
@@ -256,6 +282,7 @@ class Case:
                                                      self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j]),
         }
         if wl.mla:
+            calls["index_key"] = lambda: self._index_key(0)
             calls["mla_absorb"] = lambda: dsa.mla_absorb_q(self.q_nope, self.q_pe, self.mw.w_kvb, self.bt.q,
                                                            self.mla_ws)
             calls["mla_output"] = lambda: dsa.mla_output(self.out, self.mw.w_kvb, self.mw.w_o, self.o_mid, self.y,
@@ -291,6 +318,8 @@ class Case:
         }
         if wl.mla:
             T = self.max_rows
+            nt = len(pos)
+            work["index_key"] = dict(flop=IK_FLOP_PER_TOKEN * nt, bytes=IK_BYTES_PER_TOKEN * nt + IK_WEIGHT_BYTES)
             work["mla_absorb"] = dict(flop=ABS_FLOP_PER_TOKEN * T, bytes=ABS_BYTES_PER_TOKEN * T + ABS_WEIGHT_BYTES)
             work["mla_output"] = dict(flop=OUT_FLOP_PER_TOKEN * T, bytes=OUT_BYTES_PER_TOKEN * T + OUT_WEIGHT_BYTES)
         return work
@@ -378,12 +407,16 @@ def host_sample(case: Case, n_seq: int):
     return b, rows, len(rows), f"{len(rows)} evenly spaced query rows of the {T}-token prefill"
 
 
-def oracle_path_seconds(b, rows, attention_layers: int = 1, mla=None):
+def oracle_path_seconds(b, rows, attention_layers: int = 1, mla=None, ik=None):
     """The oracle's whole path on `rows`; attention_layers > 1 repeats the
     attention on the same indices (IndexShare's shared layers); mla =
-    (q_nope, q_pe, w_kv_b, w_o) of those rows adds the projections around it."""
+    (q_nope, q_pe, w_kv_b, w_o) of those rows adds the projections around it,
+    ik = (x, IndexKeyParams, cos, sin) the index-key producer."""
     import oracle
     t0 = time.perf_counter()
+    if ik is not None:
+        x, p, c, sn = ik
+        oracle.index_key(x, p.wk, p.gamma, p.beta, p.eps, c, sn, p.ww)
     if mla is not None:
         oracle.mla_absorb_q(mla[0], mla[1], mla[2])
     sc = oracle.indexer_scores(b, rows)
@@ -404,13 +437,17 @@ def cpu_baseline(case: Case, unit: str):
     import oracle
     n = 24 if case.wl.base == "decode" else 48
     b, rows, units, sample = host_sample(case, n)
-    mla = None
+    mla = ik = None
     if case.wl.mla:
         import torch
         ri = torch.tensor(rows, dtype=torch.long, device=case.q_nope.device)
         mla = (_bits(case.q_nope[ri]), _bits(case.q_pe[ri]), _bits(case.mw.w_kvb), _bits(case.mw.w_o))
-        sample += "; with the MLA projections"
-    secs = oracle_path_seconds(b, rows, mla=mla)
+        ip = W.IndexKeyParams(_bits(case.ik["wk"]), _bits(case.ik["ww"]), case.ik["gamma"].cpu().numpy(),
+                              case.ik["beta"].cpu().numpy(), case.ik["eps"])
+        c, sn = W.rotary_rows([case.positions[0][r] for r in rows])
+        ik = (_bits(case.x[ri]), ip, c, sn)
+        sample += "; with the index-key producer and the MLA projections"
+    secs = oracle_path_seconds(b, rows, mla=mla, ik=ik)
     # units: decode -> fraction of one step; prefill -> query rows (tokens)
     return {"value": units / secs, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": sample + f" (full path: indexer, top-k, attention; {secs:.1f} s in fp64)"}
@@ -446,15 +483,17 @@ def run_reference(args):
         rows = [int(x) for x in np.linspace(0, T - 1, nq)]
         frac = nq
         sample = f"{nq} evenly spaced query rows per timed step"
-    mla = None
+    mla = ik = None
     if wl.mla:
         mw = W.make_mla_weights_np(wl.seed + 1)
         qn, qp = W.make_mla_queries_np(len(rows), wl.seed + 2)
         mla = (qn, qp, mw.w_kvb, mw.w_o)
-        sample += "; with the MLA projections"
+        c, sn = W.rotary_rows([wl.ctx - 1] * len(rows) if wl.base == "decode" else rows)
+        ik = (W.make_hidden_np(len(rows), wl.seed + 4), W.make_index_key_params_np(wl.seed + 3), c, sn)
+        sample += "; with the index-key producer and the MLA projections"
 
     def one_step():
-        oracle_path_seconds(b, rows, 1 + shared_layers, mla=mla)
+        oracle_path_seconds(b, rows, 1 + shared_layers, mla=mla, ik=ik)
 
     for _ in range(Wu):
         one_step()
@@ -576,7 +615,8 @@ def run_dsa(args):
     peaks, peak_src = load_peaks()
     dom = max(times, key=times.get)
     kw = work[dom]
-    if wl.base not in ("decode", "indexshare") and dom in ("indexer", "sparse_mla", "mla_absorb", "mla_output"):
+    if wl.base not in ("decode", "indexshare") and dom in ("indexer", "sparse_mla", "mla_absorb", "mla_output",
+                                                         "index_key"):
         achieved = kw["flop"] / (times[dom] * 1e-6) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"]}
@@ -623,33 +663,35 @@ def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
     stream = torch.cuda.current_stream()
     # the step's query-side inputs and result: the absorbed q and the latent
     # output, or (MLA layer) q_nope / q_pe and the o_proj output y
+    # (the MLA layer produces w and the new index keys itself, from x)
     if wl.mla:
-        qside = {"q_nope": case.q_nope, "q_pe": case.q_pe}
+        qside = {"q_idx": bt.q_idx, "q_nope": case.q_nope, "q_pe": case.q_pe, "x": case.x}
         result = case.y
     else:
-        qside = {"q": bt.q}
+        qside = {"q_idx": bt.q_idx, "w": bt.w, "q": bt.q}
         result = case.out
     if wl.base == "decode":
-        host = {"q_idx": bt.q_idx.cpu().pin_memory(), "w": bt.w.cpu().pin_memory()}
-        host.update({k: v.cpu().pin_memory() for k, v in qside.items()})
+        host = {k: v.cpu().pin_memory() for k, v in qside.items()}
         kv3 = bt.kv.view(wl.B, bt.stride, 576)
         ki3 = bt.k_idx.view(wl.B, bt.stride, 128)
         new_kv = kv3[:, wl.ctx - 1].cpu().pin_memory()
         new_ki = ki3[:, wl.ctx - 1].cpu().pin_memory()
         out_h = torch.empty(result.shape, dtype=result.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + [new_kv, new_ki])
+        new_rows = [new_kv] if wl.mla else [new_kv, new_ki]
+        h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + new_rows)
         d2h = out_h.numel() * out_h.element_size()
-        dev_of = {"q_idx": bt.q_idx, "w": bt.w, **qside}
+        dev_of = qside
 
         def step(i):
             for name, t in host.items():
                 dev_of[name].copy_(t, non_blocking=True)
             kv3[:, wl.ctx - 1].copy_(new_kv, non_blocking=True)
-            ki3[:, wl.ctx - 1].copy_(new_ki, non_blocking=True)
+            if not wl.mla:
+                ki3[:, wl.ctx - 1].copy_(new_ki, non_blocking=True)
             case.step(len(case.batches) - 1)
             out_h.copy_(result, non_blocking=True)
     else:
-        dev_of = {"q_idx": bt.q_idx, "w": bt.w, "kv": bt.kv, "k_idx": bt.k_idx, **qside}
+        dev_of = dict(qside, kv=bt.kv) if wl.mla else dict(qside, kv=bt.kv, k_idx=bt.k_idx)
         host = {k: v.cpu().pin_memory() for k, v in dev_of.items()}
         out_h = torch.empty(result.shape, dtype=result.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -671,7 +713,7 @@ def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1))
     value = whole_job_value(case.units_per_step, K, world, ms)
-    api = ("sparse_attention_gb300.mla_absorb_q + forward + mla_output" if wl.mla
+    api = ("sparse_attention_gb300.index_key_producer + mla_absorb_q + forward + mla_output" if wl.mla
            else "sparse_attention_gb300.forward")
     return {"value": value, "unit": case.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": api}
 
