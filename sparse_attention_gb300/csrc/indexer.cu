@@ -14,7 +14,9 @@
 //               a ring of shared-memory stages (128B-swizzled boxes)
 //   warp 1      TMEM allocator and MMA issuer (tcgen05.mma kind::f16,
 //               bf16 x bf16 -> fp32), double-buffered accumulators
-//   warps 2..5  epilogue: tcgen05.ld one key row per thread (two queries'
+//   warps 2..    epilogue (8 warps for query groups, two per TMEM lane
+//               quarter each taking half of the queries; 4 for a single
+//               query): tcgen05.ld one key row per thread (two queries'
 //               accumulators per wait), then the ReLU and the
 //               head-weighted sum in registers (fp32, four partial sums
 //               over the heads in a fixed order), and a coalesced store of
@@ -42,8 +44,12 @@ struct IdxCfg {
     static constexpr int kBBytes = 2 * kBBoxBytes;
     static constexpr int kAcc = 2;                   // TMEM accumulator buffers
     static constexpr int kTmemCols = (kN * kAcc < 32) ? 32 : kN * kAcc;
-    static constexpr int kThreads = 192;
-    static constexpr int kEpiQ = (NQ >= 2) ? 2 : 1;    // queries read from TMEM per wait
+    // epilogue warps: two per TMEM lane quarter (each half of the queries)
+    // for query groups, one per quarter for a single query
+    static constexpr int kEpiWarps = (NQ >= 8) ? 8 : 4;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kQPerWarp = NQ * 4 / kEpiWarps;  // queries of one epilogue warp
+    static constexpr int kEpiQ = (kQPerWarp >= 2) ? 2 : 1;    // queries read from TMEM per wait
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
     static constexpr int kOffW = kOffB + kBBytes;
@@ -58,7 +64,7 @@ struct IdxCfg {
 };
 
 template <int NQ>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
     indexer_kernel(const BatchDev bd, const RowRange rr, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_q, const float* __restrict__ w,
                    float* __restrict__ scores, const int64_t ld, const int scores_local,
@@ -103,7 +109,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(bfull_bar, 1);
         for (int a = 0; a < C::kAcc; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 128);
+            mbar_init(tempty_bar(a), 32 * C::kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         misc[1] = 0;  // abort flag
@@ -115,7 +121,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (warp >= 2) {
         // head weights of the group (0 for rows past the group's end)
-        for (int e = threadIdx.x - 64; e < NQ * kHIdx; e += 128) {
+        for (int e = threadIdx.x - 64; e < NQ * kHIdx; e += 32 * C::kEpiWarps) {
             const int qi = e / kHIdx;
             w_s[e] = (qlo + qi < qhi) ? __ldg(w + ((int64_t)sq.q0 + qlo + qi) * kHIdx + (e % kHIdx)) : 0.f;
         }
@@ -209,6 +215,7 @@ __global__ void __launch_bounds__(192, 1)
         // -------------------------------------------------------- epilogue
         const uint32_t lq = warp & 3u;                     // TMEM lane quarter of this warp
         const int32_t row = (int32_t)(lq * 32 + lane);     // key row within the tile
+        const int q_first = (int)((warp - 2) >> 2) * C::kQPerWarp;   // this warp's queries
         for (int it = 0; it < niter; ++it) {
             const int a = it & 1;
             bool ok = !misc[1] && mbar_wait(tfull_bar(a), (it >> 1) & 1u);
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(192, 1)
             const int32_t s = (j0 + it) * C::kBM + row;
             const uint32_t tq = tmem_base + ((lq * 32u) << 16) + (uint32_t)(a * C::kN);
 #pragma unroll 1
-            for (int q0 = 0; q0 < NQ; q0 += kEpiQ) {
+            for (int q0 = q_first; q0 < q_first + C::kQPerWarp; q0 += kEpiQ) {
                 // kEpiQ queries' accumulators in flight before one wait
                 uint32_t r[kEpiQ][32];
 #pragma unroll
