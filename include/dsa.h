@@ -202,8 +202,9 @@ DSA_API dsa_status dsa_sparse_mla_fwd_noalloc(const dsa_batch* batch, const uint
 /* Steps 1-3 in one call (prefill, one chunk of a chunked prefill, or a
  * decode step).  idx_out [total_q, k] and scores_out [total_q, ld] are
  * optional (NULL = keep them in the workspace only); ld is ignored when
- * scores_out is NULL.  Results equal steps 1-3 called one by one, bit for
- * bit. */
+ * scores_out is NULL.  Steps 1-2 run over chunks of query rows whose scores
+ * fit in 512 MiB of the workspace; step 3 then runs once over every row.
+ * Results equal steps 1-3 called one by one, bit for bit. */
 DSA_API dsa_status dsa_forward(const dsa_batch* batch, const uint16_t* q_idx, const float* w,
                        const uint16_t* k_idx, const uint16_t* q, const uint16_t* kv, int k,
                        float sm_scale, uint16_t* out, float* lse, int32_t* idx_out,

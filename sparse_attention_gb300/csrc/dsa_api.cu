@@ -15,9 +15,12 @@ void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order
 
 namespace {
 
-// Scores of one dsa_forward chunk are sized to stay resident in the 126 MB
-// L2 between the indexer that writes them and the top-k that reads them.
-constexpr size_t kScoreChunkBytes = size_t(64) << 20;
+// Scores of one dsa_forward chunk (the workspace holds one chunk).  Fewer,
+// larger chunks cost fewer wave tails of the indexer and top-k launches than
+// keeping each chunk in L2 saves (measured: 16,384-token prefill 9.13 ms with
+// 64 MiB chunks, 8.83 ms with 512 MiB; 65,536 tokens in 8,192-token calls
+// 60.6 ms and 53.0 ms).
+constexpr size_t kScoreChunkBytes = size_t(512) << 20;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -55,11 +58,12 @@ WsLayout ws_layout(const dsa_batch* b, int k) {
     size_t off = kWsHeaderBytes;
     L.off_scores = off;
     off = round_up(off + (size_t)b->batch * rows * L.ld_s * sizeof(float), 256);
+    // indices of every query row: the attention runs once after all chunks
     L.off_idx = off;
-    off = round_up(off + (size_t)b->batch * rows * k * sizeof(int32_t), 256);
+    off = round_up(off + (size_t)b->batch * std::max(b->max_q, 1) * k * sizeof(int32_t), 256);
     L.off_attn = off;
-    // attention scratch for a forward chunk or for a whole-batch call
-    L.attn_bytes = std::max(sparse_mla_scratch_bytes(bd, rows, k), sparse_mla_scratch_bytes(bd, b->max_q, k));
+    // attention scratch for a whole-batch launch
+    L.attn_bytes = sparse_mla_scratch_bytes(bd, b->max_q, k);
     off = round_up(off + L.attn_bytes, 256);
     L.total = off;
     return L;
@@ -202,18 +206,18 @@ dsa_status dsa_forward(const dsa_batch* batch, const uint16_t* q_idx, const floa
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* sc = scores_out ? scores_out : reinterpret_cast<float*>(base + L.off_scores);
     const int64_t sc_ld = scores_out ? ld : L.ld_s;
+    // indices by packed row (idx_out, or the workspace buffer of every row)
     int32_t* ix = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + L.off_idx);
+    // scores and top-k chunk by chunk (a chunk's scores stay in L2), then
+    // one attention launch over every row (no per-chunk wave tails)
     for (int32_t i0 = 0; i0 < batch->max_q; i0 += L.chunk_rows) {
         const RowRange rr{i0, std::min(i0 + L.chunk_rows, batch->max_q)};
         cudaError_t e = launch_indexer(bd, rr, q_idx, w, k_idx, sc, sc_ld, scores_out == nullptr, status, s);
-        if (e == cudaSuccess)
-            e = launch_topk(bd, rr, sc, sc_ld, scores_out == nullptr, k, ix, idx_out == nullptr, status, s);
-        if (e == cudaSuccess)
-            e = launch_sparse_mla(bd, rr, q, kv, ix, idx_out == nullptr, k, sm_scale, out, lse, base + L.off_attn,
-                                  L.attn_bytes, status, s);
+        if (e == cudaSuccess) e = launch_topk(bd, rr, sc, sc_ld, scores_out == nullptr, k, ix, false, status, s);
         if (e != cudaSuccess) return cuda_status(e);
     }
-    return DSA_OK;
+    return cuda_status(launch_sparse_mla(bd, RowRange{0, batch->max_q}, q, kv, ix, false, k, sm_scale, out, lse,
+                                         base + L.off_attn, L.attn_bytes, status, s));
 }
 
 dsa_status dsa_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* w_kv_b,
