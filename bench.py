@@ -541,7 +541,10 @@ def traffic_from_profiles(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = {"indexer": "indexer.cu", "topk": "topk.cu", "sparse_mla": "sparse_mla.cu"}[kernel]
+    src = {"indexer": "indexer.cu", "topk": "topk.cu", "sparse_mla": "sparse_mla.cu", "mla_absorb": "mla_proj.cu",
+           "mla_output": "mla_proj.cu", "index_key": "index_key.cu"}.get(kernel)
+    if src is None:
+        return None
     with open(os.path.join(ROOT, "sparse_attention_gb300", "csrc", src), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()[:16]
     for line in open(path):

@@ -5,9 +5,11 @@ oracle's expanded path (kv_b_proj applied to every attended latent row).
 
 Tolerances: each GEMM accumulates in fp32 and rounds its result to bf16
 (relative 2^-9), so a projection is checked at |d| <= 4e-3 |ref| + 1e-4;
-o_proj reads the bf16-rounded o_mid, so y is checked tightly against o_proj
-of the GPU's own o_mid and at 1e-2 (rms + |ref|) against the oracle's y; the
-whole layer chains five bf16 roundings and is checked at 2e-2 (rms + |ref|).
+o_proj reads the bf16-rounded o_mid, whose rounding reaches y[t] in
+proportion to the rms of row t (about 2^-9 / sqrt(3) of it per element), so
+y is checked tightly against o_proj of the GPU's own o_mid and at
+1e-2 |ref| + 2e-2 rms(row) against the oracle's y; the whole layer chains
+five bf16 roundings and is checked at 2e-2 |ref| + 3e-2 rms(row).
 """
 
 import numpy as np
@@ -81,8 +83,8 @@ def test_output(weights, T):
     # o_proj of the GPU's own bf16 o_mid (numpy fp64), then the oracle's y
     y_own = _f64(o_mid) @ W.f32_from_bf16_bits(wn.w_o).astype(np.float64).T
     _close(_f64(y), y_own, 4e-3, 1e-4, "y vs o_proj(o_mid)")
-    rms = np.sqrt(np.mean(ref_y ** 2))
-    _close(_f64(y), ref_y, 1e-2, 1e-2 * rms, "y vs oracle")
+    rms = np.sqrt(np.mean(ref_y ** 2, axis=1, keepdims=True))
+    _close(_f64(y), ref_y, 1e-2, 2e-2 * rms, "y vs oracle")
 
 
 def test_layer_against_the_expanded_path(weights):
@@ -105,9 +107,10 @@ def test_layer_against_the_expanded_path(weights):
     dsa.mla_output(out, w_kvb, w_o, o_mid, y, ws)
     assert dsa.read_device_status(ws) == 0
     ref_mid, ref_y = oracle.mla_expanded(bt, qn, qp, wn.w_kvb, wn.w_o, idx.cpu().numpy())
-    rms_mid, rms_y = np.sqrt(np.mean(ref_mid ** 2)), np.sqrt(np.mean(ref_y ** 2))
-    _close(_f64(o_mid).reshape(T, 64, 256), ref_mid, 2e-2, 2e-2 * rms_mid, "o_mid vs expanded")
-    _close(_f64(y), ref_y, 2e-2, 2e-2 * rms_y, "y vs expanded")
+    rms_mid = np.sqrt(np.mean(ref_mid ** 2, axis=(1, 2), keepdims=True))
+    rms_y = np.sqrt(np.mean(ref_y ** 2, axis=1, keepdims=True))
+    _close(_f64(o_mid).reshape(T, 64, 256), ref_mid, 2e-2, 3e-2 * rms_mid, "o_mid vs expanded")
+    _close(_f64(y), ref_y, 2e-2, 3e-2 * rms_y, "y vs expanded")
 
 
 @pytest.mark.parametrize("T", [64, 16384])
@@ -134,5 +137,5 @@ def test_projections_full_size(weights, T):
     _close(_f64(q_out[ri])[:, :, :512], ref[:, :, :512], 4e-3, 1e-4, "q_lat")
     ref_mid, ref_y = oracle.mla_output(_f64(o_lat[ri]), wn.w_kvb, wn.w_o)
     _close(_f64(o_mid[ri]).reshape(len(rows), 64, 256), ref_mid, 4e-3, 1e-4, "o_mid")
-    rms = np.sqrt(np.mean(ref_y ** 2))
-    _close(_f64(y[ri]), ref_y, 1e-2, 1e-2 * rms, "y")
+    rms = np.sqrt(np.mean(ref_y ** 2, axis=1, keepdims=True))
+    _close(_f64(y[ri]), ref_y, 1e-2, 2e-2 * rms, "y")
