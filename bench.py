@@ -659,66 +659,104 @@ def run_dsa(args):
 
 
 def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
-    """Same metric through dsa.forward with the step's inputs copied in from
-    pinned host memory and the result read back, every step."""
+    """Same metric through the public API with every step's inputs copied in
+    from pinned host memory and its result read back to pinned host memory.
+    Inputs and results are double-buffered: step i + 1's host-to-device copy
+    (its own stream) overlaps step i's kernels, step i's read-back (a third
+    stream) overlaps step i + 1's."""
     import torch
     wl, bt = case.wl, case.bt
-    stream = torch.cuda.current_stream()
-    # the step's query-side inputs and result: the absorbed q and the latent
-    # output, or (MLA layer) q_nope / q_pe and the o_proj output y
-    # (the MLA layer produces w and the new index keys itself, from x)
+    comp = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(device=comp.device), torch.cuda.Stream(device=comp.device)
+    # the step's inputs (holder, attribute) and result: the absorbed q and
+    # the latent output, or (MLA layer) q_nope / q_pe / x and the o_proj
+    # output y (that layer produces w and the new index keys itself)
     if wl.mla:
-        qside = {"q_idx": bt.q_idx, "q_nope": case.q_nope, "q_pe": case.q_pe, "x": case.x}
-        result = case.y
+        names = {"q_idx": (bt, "q_idx"), "q_nope": (case, "q_nope"), "q_pe": (case, "q_pe"), "x": (case, "x")}
+        res = (case, "y")
     else:
-        qside = {"q_idx": bt.q_idx, "w": bt.w, "q": bt.q}
-        result = case.out
-    if wl.base == "decode":
-        host = {k: v.cpu().pin_memory() for k, v in qside.items()}
+        names = {"q_idx": (bt, "q_idx"), "w": (bt, "w"), "q": (bt, "q")}
+        res = (case, "out")
+    decode = wl.base == "decode"
+    if not decode:               # a prefill brings its whole caches
+        names["kv"] = (bt, "kv")
+        if not wl.mla:
+            names["k_idx"] = (bt, "k_idx")
+    host = {n: getattr(o, a).cpu().pin_memory() for n, (o, a) in names.items()}
+    bufs = [{n: getattr(o, a) for n, (o, a) in names.items()},
+            {n: torch.empty_like(getattr(o, a)) for n, (o, a) in names.items()}]
+    rbufs = [getattr(*res), torch.empty_like(getattr(*res))]
+    out_h = [torch.empty(rbufs[0].shape, dtype=rbufs[0].dtype).pin_memory() for _ in range(2)]
+    new_h, stage = [], [[], []]
+    if decode:                   # the new token's cache rows (a decode step appends them)
         kv3 = bt.kv.view(wl.B, bt.stride, 576)
         ki3 = bt.k_idx.view(wl.B, bt.stride, 128)
-        new_kv = kv3[:, wl.ctx - 1].cpu().pin_memory()
-        new_ki = ki3[:, wl.ctx - 1].cpu().pin_memory()
-        out_h = torch.empty(result.shape, dtype=result.dtype).pin_memory()
-        new_rows = [new_kv] if wl.mla else [new_kv, new_ki]
-        h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + new_rows)
-        d2h = out_h.numel() * out_h.element_size()
-        dev_of = qside
+        rows = [kv3] if wl.mla else [kv3, ki3]
+        new_h = [r[:, wl.ctx - 1].cpu().pin_memory() for r in rows]
+        stage = [[torch.empty(t.shape, dtype=t.dtype, device=comp.device) for t in new_h] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + new_h)
+    d2h = out_h[0].numel() * out_h[0].element_size()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-        def step(i):
-            for name, t in host.items():
-                dev_of[name].copy_(t, non_blocking=True)
-            kv3[:, wl.ctx - 1].copy_(new_kv, non_blocking=True)
-            if not wl.mla:
-                ki3[:, wl.ctx - 1].copy_(new_ki, non_blocking=True)
-            case.step(len(case.batches) - 1)
-            out_h.copy_(result, non_blocking=True)
-    else:
-        dev_of = dict(qside, kv=bt.kv) if wl.mla else dict(qside, kv=bt.kv, k_idx=bt.k_idx)
-        host = {k: v.cpu().pin_memory() for k, v in dev_of.items()}
-        out_h = torch.empty(result.shape, dtype=result.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_h.numel() * out_h.element_size()
+    def prefetch(i):
+        k = i % 2
+        with torch.cuda.stream(h2d_s):
+            if used[k]:
+                h2d_s.wait_event(ev_done[k])        # the step that last read buffer k has finished
+            for n, t in host.items():
+                bufs[k][n].copy_(t, non_blocking=True)
+            for dst, src in zip(stage[k], new_h):
+                dst.copy_(src, non_blocking=True)
+            ev_in[k].record(h2d_s)
 
-        def step(i):
-            for name, t in host.items():
-                dev_of[name].copy_(t, non_blocking=True)
-            case.step(i)
-            out_h.copy_(result, non_blocking=True)
-    for i in range(Wu):
-        step(i)
+    def compute(i):
+        k = i % 2
+        comp.wait_event(ev_in[k])
+        if used[k]:
+            comp.wait_event(ev_read[k])             # the read-back of result buffer k has finished
+        for n, (o, a) in names.items():
+            setattr(o, a, bufs[k][n])
+        setattr(res[0], res[1], rbufs[k])
+        if decode:
+            for r, src in zip(rows, stage[k]):
+                r[:, wl.ctx - 1].copy_(src, non_blocking=True)
+        case.step(len(case.batches) - 1 if decode else i)
+        ev_done[k].record(comp)
+        used[k] = True
+
+    def readback(i):
+        k = i % 2
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(ev_done[k])
+            out_h[k].copy_(rbufs[k], non_blocking=True)
+            ev_read[k].record(d2h_s)
+
+    def run(n):
+        prefetch(0)
+        for i in range(n):
+            compute(i)
+            if i + 1 < n:
+                prefetch(i + 1)
+            readback(i)
+        comp.wait_stream(d2h_s)
+        comp.wait_stream(h2d_s)
+
+    run(Wu)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(K):
-        step(i)
-    e1.record(stream)
+    e0.record(comp)
+    run(K)
+    e1.record(comp)
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1))
     value = whole_job_value(case.units_per_step, K, world, ms)
     api = ("sparse_attention_gb300.index_key_producer + mla_absorb_q + forward + mla_output" if wl.mla
            else "sparse_attention_gb300.forward")
-    return {"value": value, "unit": case.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": api}
+    return {"value": value, "unit": case.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": api,
+            "overlap": "double-buffered: next step's copy-in and this step's read-back overlap the kernels"}
 
 
 def main():
