@@ -14,6 +14,9 @@ Functions (all take numpy arrays; bf16 tensors as uint16 bit patterns):
   mla_output(o_lat, w_kvb, w_o)        -> (float64 [T, 64, 256], float64 [T, 6144])
   mla_expanded(batch, q_nope, q_pe, w_kvb, w_o, idx, rows) -> same pair, the pages' expanded path
   index_key(x, wk, gamma, beta, eps, cos, sin, ww) -> (float64 [T, 128], float64 [T, 32])
+  e4m3_decode(codes) / e4m3_encode(values)       -> the OCP FP8 E4M3 format
+  quantize_fp8(rows_bf16)              -> (uint8 codes, float64 scale per row)
+  indexer_scores_fp8(batch, q8, qs, k8, ks, rows) -> float64 [len(rows), ld]
 See ``oracle.c`` for what each computes and the passages it follows.
 """
 
@@ -68,6 +71,10 @@ def _load():
             lib.oracle_mla_output.argtypes = [i32, P, P, P, P, P]
             lib.oracle_mla_expanded.argtypes = [i32, P, P, i64, P, P, P, P, P, P, i32, dbl, i32, P, P, P]
             lib.oracle_index_key.argtypes = [i32, P, P, P, P, dbl, P, P, P, P, P]
+            lib.oracle_e4m3_decode_array.argtypes = [i64, P, P]
+            lib.oracle_e4m3_encode_array.argtypes = [i64, P, P]
+            lib.oracle_quantize_fp8.argtypes = [i64, ctypes.c_int, P, P, P]
+            lib.oracle_indexer_scores_fp8.argtypes = [i32, P, P, i64, P, P, P, P, P, i32, P, P, i64]
             _lib = lib
     return _lib
 
@@ -268,3 +275,50 @@ def index_key(x, wk, gamma, beta, eps, cos, sin, ww) -> Tuple[np.ndarray, np.nda
     _load().oracle_index_key(T, _ptr(xb), _ptr(wkb), _ptr(g), _ptr(b), float(eps), _ptr(c), _ptr(s), _ptr(wwb),
                              _ptr(k), _ptr(w))
     return k, w
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode_array(c.size, _ptr(c), _ptr(out))
+    return out
+
+
+def e4m3_encode(values) -> np.ndarray:
+    x = np.ascontiguousarray(np.asarray(values, dtype=np.float64))
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(x.size, _ptr(x), _ptr(out))
+    return out
+
+
+def quantize_fp8(rows_bf16, n: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Rows of n bf16 values -> (E4M3 codes [rows, n], scale [rows]) with
+    scale = amax / 448 (1 for an all-zero row)."""
+    v = _np(rows_bf16, np.uint16)
+    rows = v.size // n
+    if v.size != rows * n:
+        raise ValueError("size is not a multiple of n")
+    codes = np.empty((rows, n), dtype=np.uint8)
+    scale = np.empty(rows, dtype=np.float64)
+    _load().oracle_quantize_fp8(rows, n, _ptr(v), _ptr(codes), _ptr(scale))
+    return codes, scale
+
+
+def indexer_scores_fp8(batch, q8, qs, k8, ks, rows: Optional[Sequence[int]] = None,
+                       ld: Optional[int] = None) -> np.ndarray:
+    """Lightning-indexer scores on E4M3 queries / keys with per-(token, head)
+    and per-key scales; entries s > t are NaN."""
+    r = _rows(batch, rows)
+    ld = int(ld if ld is not None else max(batch.max_ctx, 1))
+    q8a, k8a = np.ascontiguousarray(q8, dtype=np.uint8), np.ascontiguousarray(k8, dtype=np.uint8)
+    qsa, ksa = np.ascontiguousarray(qs, dtype=np.float64), np.ascontiguousarray(ks, dtype=np.float64)
+    w = _np(batch.w, np.float32)
+    if q8a.size < batch.total_q * H_IDX * D_IDX or qsa.size < batch.total_q * H_IDX or \
+            k8a.size < batch.B * batch.stride * D_IDX or ksa.size < batch.B * batch.stride:
+        raise ValueError("FP8 arrays smaller than the batch")
+    _check_layout(batch, w=w)
+    out = np.full((len(r), ld), np.nan, dtype=np.float64)
+    q_off, ctx = _np(batch.q_off, np.int32), _np(batch.ctx_len, np.int32)
+    _load().oracle_indexer_scores_fp8(batch.B, _ptr(q_off), _ptr(ctx), int(batch.stride), _ptr(q8a), _ptr(qsa),
+                                      _ptr(w), _ptr(k8a), _ptr(ksa), len(r), _ptr(r), _ptr(out), ld)
+    return out

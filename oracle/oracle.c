@@ -65,6 +65,20 @@
  *      (the rotary table of the position embedding) and the pairing is the
  *      rotate-half one of the pages' apply_rotary_pos_emb.
  *
+ * Reduced-precision index keys (the pages give no recipe; the reading used
+ * here is stated once and followed by the GPU path):
+ *  oracle_e4m3_decode / oracle_e4m3_encode -- the OCP 8-bit floating point
+ *      E4M3 format: 1 sign, 4 exponent (bias 7), 3 mantissa bits; normals
+ *      (1 + m/8) 2^(e-7), subnormals (m/8) 2^-6, S.1111.111 is NaN, no
+ *      infinities, largest finite 448; encoding rounds to nearest, ties to
+ *      the even code, and saturates finite values beyond 448 to +-448.
+ *  oracle_quantize_fp8    -- one scale per row of n values: amax / 448 (1 when
+ *      the row is all zero); codes = encode(v / scale).  Index keys use one
+ *      row per key (128 dims), indexer queries one row per (token, head).
+ *  oracle_indexer_scores_fp8 -- the lightning-indexer score on the
+ *      dequantised values: I[t,s] = sum_h w[t,h] ReLU(sq[t,h] sk[s]
+ *      sum_d q8[t,h,d] k8[s,d]) with q8, k8 decoded exactly.
+ *
  * Plain loops, no blocking, no reordering; OpenMP only splits query rows.
  */
 #include <math.h>
@@ -439,4 +453,85 @@ void oracle_index_key(int T, const uint16_t* x, const uint16_t* wk, const double
             w_out[(int64_t)t * O_HIDX + h] = acc / sqrt((double)O_HIDX);
         }
     }
+}
+
+/* ---- E4M3 (OCP FP8) ---- */
+double oracle_e4m3_decode(uint8_t c) {
+    int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+/* Nearest E4M3 code, ties to the even code; finite values beyond 448
+ * saturate to +-448.  (Reference by exhaustive search over the 126 finite
+ * non-negative magnitudes, so no rounding arithmetic can slip.) */
+uint8_t oracle_e4m3_encode(double x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sgn = x < 0 ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sgn | 0x7E);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c < 0x7F; c++) {          /* codes 0x00 .. 0x7E: +0 .. 448 */
+        double d = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sgn | best);
+}
+
+/* rows of n bf16 values -> n codes per row and one scale per row */
+void oracle_quantize_fp8(int64_t rows, int n, const uint16_t* v, uint8_t* codes, double* scale) {
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t r = 0; r < rows; r++) {
+        double amax = 0.0;
+        for (int d = 0; d < n; d++) {
+            double a = fabs(widen_bf16(v[r * n + d]));
+            if (a > amax) amax = a;
+        }
+        double sc = amax > 0.0 ? amax / 448.0 : 1.0;
+        scale[r] = sc;
+        for (int d = 0; d < n; d++) codes[r * n + d] = oracle_e4m3_encode(widen_bf16(v[r * n + d]) / sc);
+    }
+}
+
+/* Scores of requested rows on FP8 queries / keys (row layouts as
+ * oracle_indexer_scores; q8 [total_q, 32, 128], qs [total_q, 32],
+ * k8 [B*stride, 128], ks [B*stride]). */
+void oracle_indexer_scores_fp8(int B, const int32_t* q_off, const int32_t* ctx_len, int64_t stride,
+                               const uint8_t* q8, const double* qs, const float* w, const uint8_t* k8,
+                               const double* ks, int nrows, const int32_t* rows, double* out, int64_t ld) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int j = 0; j < nrows; j++) {
+        int b;
+        int64_t t;
+        locate_row(B, q_off, ctx_len, rows[j], &b, &t);
+        for (int64_t s = 0; s <= t; s++) {
+            const uint8_t* kr = k8 + ((int64_t)b * stride + s) * O_DIDX;
+            double ksc = ks[(int64_t)b * stride + s];
+            double score = 0.0;
+            for (int h = 0; h < O_HIDX; h++) {
+                const uint8_t* qr = q8 + ((int64_t)rows[j] * O_HIDX + h) * O_DIDX;
+                double dot = 0.0;
+                for (int d = 0; d < O_DIDX; d++) dot += oracle_e4m3_decode(qr[d]) * oracle_e4m3_decode(kr[d]);
+                double x = qs[(int64_t)rows[j] * O_HIDX + h] * ksc * dot;
+                score += (double)w[(int64_t)rows[j] * O_HIDX + h] * (x > 0.0 ? x : 0.0);
+            }
+            out[(int64_t)j * ld + s] = score;
+        }
+    }
+}
+
+void oracle_e4m3_decode_array(int64_t n, const uint8_t* c, double* out) {
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_decode(c[i]);
+}
+
+void oracle_e4m3_encode_array(int64_t n, const double* x, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_encode(x[i]);
 }
