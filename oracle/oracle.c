@@ -73,8 +73,9 @@
  *      infinities, largest finite 448; encoding rounds to nearest, ties to
  *      the even code, and saturates finite values beyond 448 to +-448.
  *  oracle_quantize_fp8    -- one scale per row of n values: amax / 448 (1 when
- *      the row is all zero); codes = encode(v / scale).  Index keys use one
- *      row per key (128 dims), indexer queries one row per (token, head).
+ *      the row is all zero); codes = encode(v / scale), scale and quotient
+ *      in single precision.  Index keys use one row per key (128 dims),
+ *      indexer queries one row per (token, head).
  *  oracle_indexer_scores_fp8 -- the lightning-indexer score on the
  *      dequantised values: I[t,s] = sum_h w[t,h] ReLU(sq[t,h] sk[s]
  *      sum_d q8[t,h,d] k8[s,d]) with q8, k8 decoded exactly.
@@ -485,18 +486,24 @@ uint8_t oracle_e4m3_encode(double x) {
     return (uint8_t)(sgn | best);
 }
 
-/* rows of n bf16 values -> n codes per row and one scale per row */
+/* rows of n bf16 values -> n codes per row and one scale per row.  The
+ * scale amax / 448 and each quotient v / scale are single-precision (IEEE
+ * round to nearest) values: the code is an integer decided by floating
+ * point, so it is decided in the precision the GPU path uses. */
 void oracle_quantize_fp8(int64_t rows, int n, const uint16_t* v, uint8_t* codes, double* scale) {
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t r = 0; r < rows; r++) {
-        double amax = 0.0;
+        float amax = 0.0f;
         for (int d = 0; d < n; d++) {
-            double a = fabs(widen_bf16(v[r * n + d]));
+            float a = (float)fabs(widen_bf16(v[r * n + d]));
             if (a > amax) amax = a;
         }
-        double sc = amax > 0.0 ? amax / 448.0 : 1.0;
-        scale[r] = sc;
-        for (int d = 0; d < n; d++) codes[r * n + d] = oracle_e4m3_encode(widen_bf16(v[r * n + d]) / sc);
+        volatile float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[r] = (double)sc;
+        for (int d = 0; d < n; d++) {
+            volatile float q = (float)widen_bf16(v[r * n + d]) / sc;
+            codes[r * n + d] = oracle_e4m3_encode((double)q);
+        }
     }
 }
 

@@ -56,7 +56,8 @@ def test_quantize_scales_to_448_and_bounds_the_error():
     assert scale[7] == 1.0 and np.all(codes[7] == 0)
     amax = np.abs(xf).max(axis=1)
     ok = amax > 0
-    assert np.allclose(np.abs(deq[ok]).max(axis=1), amax[ok], rtol=1e-12)   # the largest maps to +-448 exactly
+    # the largest maps to +-448; the single-precision scale keeps 448 * scale within 2^-23 of amax
+    assert np.allclose(np.abs(deq[ok]).max(axis=1), amax[ok], rtol=2.0 ** -22)
     # nearest rounding: within half a step (2^-4 relative for normals, 2^-10 * scale for subnormals)
     err = np.abs(deq - xf)
     assert np.all(err <= np.maximum(np.abs(xf) * 2.0 ** -4, scale[:, None] * 2.0 ** -10) * (1 + 1e-12))
