@@ -289,6 +289,38 @@ DSA_API dsa_status dsa_index_key_producer(const dsa_batch* batch, const uint16_t
                                           const float* sin, const uint16_t* w_proj, uint16_t* k_idx, float* w_out,
                                           void* ws, size_t ws_bytes, void* stream);
 
+/* ---- Reduced-precision index keys.  The pages give no FP8 recipe for the
+ * indexer (only that weights_proj stays in fp32 / bf16); this library's
+ * reading: E4M3 (the OCP 8-bit format: 4 exponent bits, bias 7, 3 mantissa
+ * bits, largest finite 448) with one fp32 scale per 128-value row --
+ * amax / 448 (1 for an all-zero row) -- per cached index key and per
+ * (token, head) of the indexer queries.  Both scales are positive, so
+ *   I[t,s] = ks[s] * sum_h (w[t,h] qs[t,h]) ReLU(q8[t,h] . k8[s])
+ * with exact E4M3 products accumulated in fp32 on the tensor cores.  The
+ * index-key cache then takes 132 bytes per token instead of 256. */
+
+/* codes[r, :] = E4M3(in[r, :] / scale[r]), scale[r] = amax_r / 448 (fp32;
+ * quotients in fp32, round to nearest even, saturating at +-448).
+ *   in     bf16 [rows, 128] (DEVICE)    index keys or indexer queries
+ *   codes  uint8 [rows, 128] (DEVICE)   scale fp32 [rows] (DEVICE)
+ * 16-byte aligned pointers; rows < 0 -> DSA_ERR_INVALID_ARG. */
+DSA_API dsa_status dsa_quantize_fp8(int64_t rows, const uint16_t* in, uint8_t* codes, float* scale, void* stream);
+
+/* Step 1 on E4M3 queries and keys:
+ *   q8 uint8 [total_q, 32, 128], qs fp32 [total_q, 32]   (dsa_quantize_fp8 of q_idx)
+ *   k8 uint8 [batch * cache_stride, 128], ks fp32 [batch * cache_stride]
+ *   w, scores, ld, ws: as dsa_indexer_scores. */
+DSA_API dsa_status dsa_indexer_scores_fp8(const dsa_batch* batch, const uint8_t* q8, const float* qs,
+                                          const float* w, const uint8_t* k8, const float* ks, float* scores,
+                                          int64_t ld, void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 1-3 with E4M3 index keys (inputs of step 1 as
+ * dsa_indexer_scores_fp8, the rest as dsa_forward). */
+DSA_API dsa_status dsa_forward_fp8(const dsa_batch* batch, const uint8_t* q8, const float* qs, const float* w,
+                                   const uint8_t* k8, const float* ks, const uint16_t* q, const uint16_t* kv, int k,
+                                   float sm_scale, uint16_t* out, float* lse, int32_t* idx_out, float* scores_out,
+                                   int64_t ld, void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

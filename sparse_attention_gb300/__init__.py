@@ -33,7 +33,7 @@ STATUS = {
 EXPORTS = ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count", "dsa_workspace_size", "dsa_reset_device_status", "dsa_read_device_status",
            "dsa_selftest_wait_timeout", "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_fwd",
            "dsa_sparse_mla_fwd_noalloc", "dsa_forward", "dsa_mla_absorb_q", "dsa_mla_workspace_size", "dsa_mla_output", "dsa_index_key_workspace_size",
-           "dsa_index_key_producer")
+           "dsa_index_key_producer", "dsa_quantize_fp8", "dsa_indexer_scores_fp8", "dsa_forward_fp8")
 
 
 class DsaError(RuntimeError):
@@ -85,6 +85,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_mla_workspace_size.argtypes = [i32, ctypes.POINTER(sz)]
     lib.dsa_index_key_workspace_size.argtypes = [i32, ctypes.POINTER(sz)]
     lib.dsa_index_key_producer.argtypes = [BP, P, P, P, P, f32, P, P, P, P, P, P, sz, P]
+    lib.dsa_quantize_fp8.argtypes = [i64, P, P, P, P]
+    lib.dsa_indexer_scores_fp8.argtypes = [BP, P, P, P, P, P, P, i64, P, sz, P]
+    lib.dsa_forward_fp8.argtypes = [BP, P, P, P, P, P, P, P, i32, f32, P, P, P, P, i64, P, sz, P]
     for name in EXPORTS:
         if name not in ("dsa_status_string", "dsa_last_cuda_error", "dsa_kernel_launch_count"):
             getattr(lib, name).restype = ctypes.c_int
@@ -289,3 +292,31 @@ def index_key_producer(batch: Batch, x, wk, gamma, beta, eps: float, cos, sin, w
                                                  _p(w_out), _p(ws), ws.numel(), _stream(stream)),
            "dsa_index_key_producer")
     return k_idx
+
+
+def quantize_fp8(x, codes, scale, stream=None):
+    """E4M3 codes and per-row scales of bf16 rows of 128 (see dsa_quantize_fp8)."""
+    assert codes.dtype == torch.uint8 and scale.dtype == torch.float32
+    rows = x.numel() // 128
+    _check(load_library().dsa_quantize_fp8(int(rows), _bf16(x), _p(codes), _p(scale), _stream(stream)),
+           "dsa_quantize_fp8")
+    return codes, scale
+
+
+def indexer_scores_fp8(batch: Batch, q8, qs, w, k8, ks, scores, ld: Optional[int] = None, ws=None, stream=None):
+    ld = int(ld if ld is not None else scores.shape[-1])
+    _check(load_library().dsa_indexer_scores_fp8(ctypes.byref(batch.c), _p(q8), _p(qs), _p(w), _p(k8), _p(ks),
+                                                 _p(scores), ld, _p(ws), ws.numel() if ws is not None else 0,
+                                                 _stream(stream)), "dsa_indexer_scores_fp8")
+    return scores
+
+
+def forward_fp8(batch: Batch, q8, qs, w, k8, ks, q, kv, k: int, sm_scale: float, out, lse=None, idx_out=None,
+                scores_out=None, ld: int = 0, ws=None, stream=None):
+    if scores_out is not None and not ld:
+        ld = scores_out.shape[-1]
+    _check(load_library().dsa_forward_fp8(ctypes.byref(batch.c), _p(q8), _p(qs), _p(w), _p(k8), _p(ks), _bf16(q),
+                                          _bf16(kv), int(k), float(sm_scale), _bf16(out), _p(lse), _p(idx_out),
+                                          _p(scores_out), int(ld), _p(ws), ws.numel() if ws is not None else 0,
+                                          _stream(stream)), "dsa_forward_fp8")
+    return out

@@ -89,6 +89,54 @@ dsa_status check_ws(const dsa_batch* b, int k, void* ws, size_t ws_bytes) {
 
 using namespace dsa;
 
+namespace {
+
+// Steps 1-3: `score(rr, scores, ld, local)` runs the indexer over the local
+// query rows rr (bf16 or E4M3 keys); the rest is shared.
+template <typename ScoreFn>
+dsa_status forward_impl(const dsa_batch* batch, ScoreFn score, const uint16_t* q, const uint16_t* kv, int k,
+                        float sm_scale, uint16_t* out, float* lse, int32_t* idx_out, float* scores_out, int64_t ld,
+                        void* ws, cudaStream_t s) {
+    const BatchDev bd = to_dev(batch);
+    const WsLayout L = ws_layout(batch, k);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int32_t* status = static_cast<int32_t*>(ws);
+    float* sc = scores_out ? scores_out : reinterpret_cast<float*>(base + L.off_scores);
+    const int64_t sc_ld = scores_out ? ld : L.ld_s;
+    // indices by packed row (idx_out, or the workspace buffer of every row)
+    int32_t* ix = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + L.off_idx);
+    // scores and top-k chunk by chunk, then one attention launch over every
+    // row (no per-chunk wave tails)
+    for (int32_t i0 = 0; i0 < batch->max_q; i0 += L.chunk_rows) {
+        const RowRange rr{i0, std::min(i0 + L.chunk_rows, batch->max_q)};
+        cudaError_t e = score(rr, sc, sc_ld, scores_out == nullptr);
+        if (e == cudaSuccess) e = launch_topk(bd, rr, sc, sc_ld, scores_out == nullptr, k, ix, false, status, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return cuda_status(launch_sparse_mla(bd, RowRange{0, batch->max_q}, q, kv, ix, false, k, sm_scale, out, lse,
+                                         base + L.off_attn, L.attn_bytes, status, s));
+}
+
+// Host checks shared by the forward calls (everything but the indexer inputs).
+dsa_status check_forward(const dsa_batch* batch, const uint16_t* q, const uint16_t* kv, int k, float sm_scale,
+                         const uint16_t* out, const float* lse, const int32_t* idx_out, const float* scores_out,
+                         int64_t ld, void* ws, size_t ws_bytes) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+    if ((st = check_ws(batch, k, ws, ws_bytes)) != DSA_OK) return st;
+    if (batch->total_q == 0 || batch->max_q == 0) return DSA_OK;
+    if (!q || !kv || !out) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || (lse && !aligned16(lse)) ||
+        (idx_out && !aligned16(idx_out)) || (scores_out && !aligned16(scores_out)))
+        return DSA_ERR_INVALID_ARG;
+    if (scores_out && (ld < batch->max_ctx || ld % 4 != 0)) return DSA_ERR_INVALID_ARG;
+    if (!(sm_scale > 0.f) || sm_scale == INFINITY) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* dsa_status_string(int s) {
@@ -186,38 +234,61 @@ dsa_status dsa_sparse_mla_fwd(const dsa_batch* batch, const uint16_t* q, const u
 dsa_status dsa_forward(const dsa_batch* batch, const uint16_t* q_idx, const float* w, const uint16_t* k_idx,
                        const uint16_t* q, const uint16_t* kv, int k, float sm_scale, uint16_t* out, float* lse,
                        int32_t* idx_out, float* scores_out, int64_t ld, void* ws, size_t ws_bytes, void* stream) {
-    dsa_status st = check_batch(batch);
-    if (st != DSA_OK) return st;
-    if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
-    if ((st = check_ws(batch, k, ws, ws_bytes)) != DSA_OK) return st;
-    if (batch->total_q == 0 || batch->max_q == 0) return DSA_OK;
-    if (!q_idx || !w || !k_idx || !q || !kv || !out) return DSA_ERR_INVALID_ARG;
-    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q) || !aligned16(kv) ||
-        !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)) ||
-        (scores_out && !aligned16(scores_out)))
-        return DSA_ERR_INVALID_ARG;
-    if (scores_out && (ld < batch->max_ctx || ld % 4 != 0)) return DSA_ERR_INVALID_ARG;
-    if (!(sm_scale > 0.f) || sm_scale == INFINITY) return DSA_ERR_INVALID_ARG;
-
+    dsa_status st = check_forward(batch, q, kv, k, sm_scale, out, lse, idx_out, scores_out, ld, ws, ws_bytes);
+    if (st != DSA_OK || batch->total_q == 0 || batch->max_q == 0) return st;
+    if (!q_idx || !w || !k_idx || !aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx)) return DSA_ERR_INVALID_ARG;
     const BatchDev bd = to_dev(batch);
-    const WsLayout L = ws_layout(batch, k);
-    uint8_t* base = static_cast<uint8_t*>(ws);
     int32_t* status = static_cast<int32_t*>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    float* sc = scores_out ? scores_out : reinterpret_cast<float*>(base + L.off_scores);
-    const int64_t sc_ld = scores_out ? ld : L.ld_s;
-    // indices by packed row (idx_out, or the workspace buffer of every row)
-    int32_t* ix = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + L.off_idx);
-    // scores and top-k chunk by chunk (a chunk's scores stay in L2), then
-    // one attention launch over every row (no per-chunk wave tails)
-    for (int32_t i0 = 0; i0 < batch->max_q; i0 += L.chunk_rows) {
-        const RowRange rr{i0, std::min(i0 + L.chunk_rows, batch->max_q)};
-        cudaError_t e = launch_indexer(bd, rr, q_idx, w, k_idx, sc, sc_ld, scores_out == nullptr, status, s);
-        if (e == cudaSuccess) e = launch_topk(bd, rr, sc, sc_ld, scores_out == nullptr, k, ix, false, status, s);
-        if (e != cudaSuccess) return cuda_status(e);
-    }
-    return cuda_status(launch_sparse_mla(bd, RowRange{0, batch->max_q}, q, kv, ix, false, k, sm_scale, out, lse,
-                                         base + L.off_attn, L.attn_bytes, status, s));
+    return forward_impl(
+        batch,
+        [&](RowRange rr, float* sc, int64_t sld, bool local) {
+            return launch_indexer(bd, rr, q_idx, w, k_idx, sc, sld, local, status, s);
+        },
+        q, kv, k, sm_scale, out, lse, idx_out, scores_out, ld, ws, s);
+}
+
+dsa_status dsa_forward_fp8(const dsa_batch* batch, const uint8_t* q8, const float* qs, const float* w,
+                           const uint8_t* k8, const float* ks, const uint16_t* q, const uint16_t* kv, int k,
+                           float sm_scale, uint16_t* out, float* lse, int32_t* idx_out, float* scores_out, int64_t ld,
+                           void* ws, size_t ws_bytes, void* stream) {
+    dsa_status st = check_forward(batch, q, kv, k, sm_scale, out, lse, idx_out, scores_out, ld, ws, ws_bytes);
+    if (st != DSA_OK || batch->total_q == 0 || batch->max_q == 0) return st;
+    if (!q8 || !qs || !w || !k8 || !ks || !aligned16(q8) || !aligned16(qs) || !aligned16(w) || !aligned16(k8) ||
+        !aligned16(ks))
+        return DSA_ERR_INVALID_ARG;
+    const BatchDev bd = to_dev(batch);
+    int32_t* status = static_cast<int32_t*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return forward_impl(
+        batch,
+        [&](RowRange rr, float* sc, int64_t sld, bool local) {
+            return launch_indexer_fp8(bd, rr, q8, qs, w, k8, ks, sc, sld, local, status, s);
+        },
+        q, kv, k, sm_scale, out, lse, idx_out, scores_out, ld, ws, s);
+}
+
+dsa_status dsa_indexer_scores_fp8(const dsa_batch* batch, const uint8_t* q8, const float* qs, const float* w,
+                                  const uint8_t* k8, const float* ks, float* scores, int64_t ld, void* ws,
+                                  size_t ws_bytes, void* stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (!ws || !aligned16(ws) || ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
+    if (batch->total_q == 0 || batch->max_q == 0) return DSA_OK;
+    if (!q8 || !qs || !w || !k8 || !ks || !scores) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q8) || !aligned16(qs) || !aligned16(w) || !aligned16(k8) || !aligned16(ks) || !aligned16(scores))
+        return DSA_ERR_INVALID_ARG;
+    if (ld < batch->max_ctx || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
+    return cuda_status(launch_indexer_fp8(to_dev(batch), RowRange{0, batch->max_q}, q8, qs, w, k8, ks, scores, ld,
+                                          false, static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_quantize_fp8(int64_t rows, const uint16_t* in, uint8_t* codes, float* scale, void* stream) {
+    if (rows < 0) return DSA_ERR_INVALID_ARG;
+    if (rows == 0) return DSA_OK;
+    if (!in || !codes || !scale || !aligned16(in) || !aligned16(codes) || !aligned16(scale))
+        return DSA_ERR_INVALID_ARG;
+    return cuda_status(launch_quantize_fp8(rows, in, codes, scale, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* w_kv_b,

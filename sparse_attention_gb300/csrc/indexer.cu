@@ -33,15 +33,20 @@
 namespace dsa {
 namespace {
 
-template <int NQ>
+// NQ queries per group; kFp8: E4M3 queries and keys with scales (else bf16).
+template <int NQ, bool kFp8 = false>
 struct IdxCfg {
     static constexpr int kN = NQ * kHIdx;            // MMA N: queries x heads
     static constexpr int kBM = 128;                  // keys per tile: MMA M
     static constexpr int kStages = (NQ == 1) ? 3 : 4;
-    static constexpr int kABoxBytes = kBM * 64 * 2;  // 64 of the 128 dims, 16 KiB
-    static constexpr int kABytes = 2 * kABoxBytes;
-    static constexpr int kBBoxBytes = kN * 64 * 2;
-    static constexpr int kBBytes = 2 * kBBoxBytes;
+    // a key row is 128 dims: two 64-element boxes of bf16 or one 128-element
+    // box of E4M3, 128 bytes per row either way
+    static constexpr int kBoxes = kFp8 ? 1 : 2;
+    static constexpr int kBoxElems = kFp8 ? 128 : 64;
+    static constexpr int kABoxBytes = kBM * 128;     // 16 KiB
+    static constexpr int kABytes = kBoxes * kABoxBytes;
+    static constexpr int kBBoxBytes = kN * 128;
+    static constexpr int kBBytes = kBoxes * kBBoxBytes;
     static constexpr int kAcc = 2;                   // TMEM accumulator buffers
     static constexpr int kTmemCols = (kN * kAcc < 32) ? 32 : kN * kAcc;
     // epilogue warps: two per TMEM lane quarter (each half of the queries)
@@ -63,13 +68,14 @@ struct IdxCfg {
     static_assert(kN % 16 == 0 && kN >= 16 && kN <= 256, "invalid MMA N for M = 128");
 };
 
-template <int NQ>
-__global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
+template <int NQ, bool kFp8>
+__global__ void __launch_bounds__(IdxCfg<NQ, kFp8>::kThreads, 1)
     indexer_kernel(const BatchDev bd, const RowRange rr, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_q, const float* __restrict__ w,
+                   const float* __restrict__ qscale, const float* __restrict__ kscale,
                    float* __restrict__ scores, const int64_t ld, const int scores_local,
                    const int tiles_per_split, int32_t* status) {
-    using C = IdxCfg<NQ>;
+    using C = IdxCfg<NQ, kFp8>;
     constexpr int kEpiQ = C::kEpiQ;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -123,7 +129,10 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
         // head weights of the group (0 for rows past the group's end)
         for (int e = threadIdx.x - 64; e < NQ * kHIdx; e += 32 * C::kEpiWarps) {
             const int qi = e / kHIdx;
-            w_s[e] = (qlo + qi < qhi) ? __ldg(w + ((int64_t)sq.q0 + qlo + qi) * kHIdx + (e % kHIdx)) : 0.f;
+            const int64_t wi = ((int64_t)sq.q0 + qlo + qi) * kHIdx + (e % kHIdx);
+            // E4M3 queries: the positive scale of each (token, head) passes
+            // through the ReLU and folds into the head weight
+            w_s[e] = (qlo + qi < qhi) ? __ldg(w + wi) * (kFp8 ? __ldg(qscale + wi) : 1.f) : 0.f;
         }
     }
     tc_fence_before();
@@ -138,8 +147,9 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
             prefetch_tmap(&tm_q);
             const int32_t qrow = (sq.q0 + qlo) * kHIdx;
             mbar_arrive_expect_tx(bfull_bar, C::kBBytes);
-            tma_load_2d(sB, &tm_q, bfull_bar, 0, qrow);
-            tma_load_2d(sB + C::kBBoxBytes, &tm_q, bfull_bar, 64, qrow);
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                tma_load_2d(sB + bx * C::kBBoxBytes, &tm_q, bfull_bar, bx * C::kBoxElems, qrow);
             // one query group per sequence: every key is read by one CTA only,
             // so the stream is marked evict-first and the scores produced
             // from it stay in L2 for the top-k
@@ -156,12 +166,11 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
                 }
                 const int32_t krow = (int32_t)((int64_t)b * bd.stride + (int64_t)(j0 + it) * C::kBM);
                 mbar_arrive_expect_tx(full_bar(s), C::kABytes);
-                if (once) {
-                    tma_load_2d_hint(sA + s * C::kABytes, &tm_k, full_bar(s), 0, krow, pol);
-                    tma_load_2d_hint(sA + s * C::kABytes + C::kABoxBytes, &tm_k, full_bar(s), 64, krow, pol);
-                } else {
-                    tma_load_2d(sA + s * C::kABytes, &tm_k, full_bar(s), 0, krow);
-                    tma_load_2d(sA + s * C::kABytes + C::kABoxBytes, &tm_k, full_bar(s), 64, krow);
+#pragma unroll
+                for (int bx = 0; bx < C::kBoxes; ++bx) {
+                    const uint32_t dst = sA + s * C::kABytes + bx * C::kABoxBytes;
+                    if (once) tma_load_2d_hint(dst, &tm_k, full_bar(s), bx * C::kBoxElems, krow, pol);
+                    else tma_load_2d(dst, &tm_k, full_bar(s), bx * C::kBoxElems, krow);
                 }
                 ++issued;
             }
@@ -176,7 +185,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (elect_one()) {
-            constexpr uint32_t idesc = idesc_bf16_f32(C::kBM, C::kN);
+            constexpr uint32_t idesc = kFp8 ? idesc_e4m3_f32(C::kBM, C::kN) : idesc_bf16_f32(C::kBM, C::kN);
             bool ok = mbar_wait(bfull_bar, 0);
             tc_fence_after();
             for (int it = 0; ok && it < niter; ++it) {
@@ -190,13 +199,14 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(a * C::kN);
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
+                for (int kb = 0; kb < C::kBoxes; ++kb) {
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
+                    for (int ks = 0; ks < 4; ++ks) {       // 32 bytes of K per instruction
                         const uint64_t ad =
                             sdesc_sw128(sA + s * C::kABytes + kb * C::kABoxBytes + ks * 32, 16, 1024);
                         const uint64_t bdsc = sdesc_sw128(sB + kb * C::kBBoxBytes + ks * 32, 16, 1024);
-                        mma_bf16_ss(d, ad, bdsc, idesc, (kb | ks) != 0);
+                        if (kFp8) mma_f8_ss(d, ad, bdsc, idesc, (kb | ks) != 0);
+                        else mma_bf16_ss(d, ad, bdsc, idesc, (kb | ks) != 0);
                     }
                 }
                 mma_commit(empty_bar(s));
@@ -228,6 +238,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
             tc_fence_after();
             const int32_t s = (j0 + it) * C::kBM + row;
             const uint32_t tq = tmem_base + ((lq * 32u) << 16) + (uint32_t)(a * C::kN);
+            // E4M3 keys: the key's positive scale multiplies its whole score
+            const float kmul = kFp8 && s <= pos0 + qhi - 1 ? __ldg(kscale + (int64_t)b * bd.stride + s) : 1.f;
 #pragma unroll 1
             for (int q0 = q_first; q0 < q_first + C::kQPerWarp; q0 += kEpiQ) {
                 // kEpiQ queries' accumulators in flight before one wait
@@ -249,7 +261,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
                         acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(r[u][4 * m + 2]), 0.f), acc[2]);
                         acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(r[u][4 * m + 3]), 0.f), acc[3]);
                     }
-                    const float v = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                    const float v = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * kmul;
                     if (i < qhi && s <= pos0 + i) scores[buf_row(scores_local, sq, b, i, rr) * ld + s] = v;
                 }
             }
@@ -266,11 +278,11 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::kThreads, 1)
     }
 }
 
-template <int NQ>
-cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, const float* w,
-                      const uint16_t* k_idx, float* scores, int64_t ld, bool scores_local, int32_t* status,
-                      cudaStream_t stream) {
-    using C = IdxCfg<NQ>;
+template <int NQ, bool kFp8>
+cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const void* q_idx, const float* qs, const float* w,
+                      const void* k_idx, const float* ks, float* scores, int64_t ld, bool scores_local,
+                      int32_t* status, cudaStream_t stream) {
+    using C = IdxCfg<NQ, kFp8>;
     const int32_t rows_per_seq = min(rr.i1, bd.max_q) - rr.i0;
     if (rows_per_seq <= 0 || bd.max_ctx <= 0) return cudaSuccess;
     const int32_t groups = (rows_per_seq + NQ - 1) / NQ;
@@ -286,16 +298,18 @@ cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, co
     }
     const int32_t splits = (tiles + tps - 1) / tps;
     CUtensorMap tm_k, tm_q;
-    if (!make_tmap_bf16_2d(&tm_k, k_idx, kDIdx, (uint64_t)bd.B * (uint64_t)bd.stride, 64, C::kBM))
-        return cudaErrorInvalidValue;
-    if (!make_tmap_bf16_2d(&tm_q, q_idx, kDIdx, (uint64_t)bd.total_q * kHIdx, 64, C::kN))
-        return cudaErrorInvalidValue;
-    cudaError_t e =
-        cudaFuncSetAttribute(indexer_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    const uint64_t krows = (uint64_t)bd.B * (uint64_t)bd.stride, qrows = (uint64_t)bd.total_q * kHIdx;
+    const bool ok = kFp8 ? make_tmap_u8_2d(&tm_k, k_idx, kDIdx, krows, C::kBoxElems, C::kBM) &&
+                               make_tmap_u8_2d(&tm_q, q_idx, kDIdx, qrows, C::kBoxElems, C::kN)
+                         : make_tmap_bf16_2d(&tm_k, k_idx, kDIdx, krows, C::kBoxElems, C::kBM) &&
+                               make_tmap_bf16_2d(&tm_q, q_idx, kDIdx, qrows, C::kBoxElems, C::kN);
+    if (!ok) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(indexer_kernel<NQ, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(splits, groups, bd.B);
-    indexer_kernel<NQ><<<grid, C::kThreads, C::kSmemBytes, stream>>>(bd, rr, tm_k, tm_q, w, scores, ld,
-                                                                      scores_local ? 1 : 0, tps, status);
+    indexer_kernel<NQ, kFp8><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+        bd, rr, tm_k, tm_q, w, qs, ks, scores, ld, scores_local ? 1 : 0, tps, status);
     const cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
@@ -307,8 +321,48 @@ cudaError_t launch_indexer(const BatchDev& bd, RowRange rr, const uint16_t* q_id
                            const uint16_t* k_idx, float* scores, int64_t ld, bool scores_local,
                            int32_t* status, cudaStream_t stream) {
     if (bd.max_q >= 16)
-        return launch_nq<8>(bd, rr, q_idx, w, k_idx, scores, ld, scores_local, status, stream);
-    return launch_nq<1>(bd, rr, q_idx, w, k_idx, scores, ld, scores_local, status, stream);
+        return launch_nq<8, false>(bd, rr, q_idx, nullptr, w, k_idx, nullptr, scores, ld, scores_local, status,
+                                   stream);
+    return launch_nq<1, false>(bd, rr, q_idx, nullptr, w, k_idx, nullptr, scores, ld, scores_local, status, stream);
+}
+
+cudaError_t launch_indexer_fp8(const BatchDev& bd, RowRange rr, const uint8_t* q8, const float* qs, const float* w,
+                               const uint8_t* k8, const float* ks, float* scores, int64_t ld, bool scores_local,
+                               int32_t* status, cudaStream_t stream) {
+    if (bd.max_q >= 16)
+        return launch_nq<8, true>(bd, rr, q8, qs, w, k8, ks, scores, ld, scores_local, status, stream);
+    return launch_nq<1, true>(bd, rr, q8, qs, w, k8, ks, scores, ld, scores_local, status, stream);
+}
+
+// One warp per row of 128 values: amax -> scale = amax / 448 (1 for a zero
+// row), codes = E4M3(v / scale) by the hardware's round-to-nearest-even
+// conversion with saturation to +-448.
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(int64_t rows, const uint16_t* __restrict__ in,
+                                                           uint8_t* __restrict__ codes, float* __restrict__ scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const uint2 raw = reinterpret_cast<const uint2*>(in + r * kDIdx)[lane];     // 4 bf16 values
+    float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                  __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(__fdiv_rn(v[1], sc)), "f"(__fdiv_rn(v[0], sc)));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(__fdiv_rn(v[3], sc)), "f"(__fdiv_rn(v[2], sc)));
+    reinterpret_cast<uint32_t*>(codes + r * kDIdx)[lane] = (uint32_t)lo | ((uint32_t)hi << 16);
+    if (lane == 0) scale[r] = sc;
+}
+
+cudaError_t launch_quantize_fp8(int64_t rows, const uint16_t* in, uint8_t* codes, float* scale, cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+    const int warps = 8;
+    quantize_fp8_kernel<<<(unsigned)((rows + warps - 1) / warps), 32 * warps, 0, stream>>>(rows, in, codes, scale);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
 }
 
 }  // namespace dsa

@@ -72,6 +72,10 @@ __device__ __forceinline__ int64_t buf_row(bool local, const SeqInfo& s, int b, 
 bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                        uint32_t box_rows);
 
+// The same for a 2-D tensor of bytes (row stride inner bytes).
+bool make_tmap_u8_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                     uint32_t box_rows);
+
 // Adds n to the process-wide count of kernels launched by this library.
 void count_launches(int n);
 
@@ -80,6 +84,13 @@ void count_launches(int n);
 cudaError_t launch_indexer(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, const float* w,
                            const uint16_t* k_idx, float* scores, int64_t ld, bool scores_local,
                            int32_t* status, cudaStream_t stream);
+
+// FP8 (E4M3) index keys: scores from quantized queries / keys (qs per
+// (token, head), ks per cached key), and the row quantizer.
+cudaError_t launch_indexer_fp8(const BatchDev& bd, RowRange rr, const uint8_t* q8, const float* qs, const float* w,
+                               const uint8_t* k8, const float* ks, float* scores, int64_t ld, bool scores_local,
+                               int32_t* status, cudaStream_t stream);
+cudaError_t launch_quantize_fp8(int64_t rows, const uint16_t* in, uint8_t* codes, float* scale, cudaStream_t stream);
 
 cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, int64_t ld,
                         bool scores_local, int k, int32_t* idx, bool idx_local, int32_t* status,

@@ -197,6 +197,17 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The same for 8-bit operands (kind::f8f6f4; K = 32 per instruction, so a
+// K step is still 32 bytes of a 128-byte row).
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -273,6 +284,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
            | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((N >> 3) << 17)               // N / 8
            | ((M >> 4) << 24);            // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0),
+// both K-major, fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+    return (1u << 4)                      // D format: f32
+           | (0u << 7) | (0u << 10)       // A, B format: E4M3
+           | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand whose

@@ -110,6 +110,13 @@ def test_compute_entry_points_reject_bad_host_arguments(lib):
     assert lib.dsa_index_key_producer(B, p, p, p, p, ctypes.c_float(0.0), p, p, p, p, p, ws, m.value, None) == 1
     assert lib.dsa_index_key_producer(B, p, None, p, p, ctypes.c_float(1e-5), p, p, p, p, p, ws, m.value, None) == 1
     assert lib.dsa_index_key_producer(B, p, p, p, bad, ctypes.c_float(1e-5), p, p, p, p, p, ws, m.value, None) == 1
+    # FP8 index keys: quantizer and forward host checks
+    assert lib.dsa_quantize_fp8(-1, p, p, p, None) == 1
+    assert lib.dsa_quantize_fp8(4, bad, p, p, None) == 1
+    assert lib.dsa_quantize_fp8(0, None, None, None, None) == 0
+    assert lib.dsa_indexer_scores_fp8(B, p, p, p, p, None, p, 16, ws, n, None) == 1
+    assert lib.dsa_forward_fp8(B, p, p, p, p, p, p, p, 8, ctypes.c_float(0.0625), p, None, None, None, 0, ws, n - 256,
+                               None) == 3
     # status word helpers check their pointers on the host
     assert lib.dsa_read_device_status(None, None, None) == 1
     assert lib.dsa_reset_device_status(None, None) == 3
