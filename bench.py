@@ -43,6 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 IDX_FLOP_PER_PAIR = 2 * 32 * 128            # 8192
 IDX_BYTES_PER_KEY = 128 * 2                 # one bf16 index key
 IDX_BYTES_PER_QUERY = 32 * 128 * 2 + 32 * 4  # q_idx + w
+IDX8_BYTES_PER_KEY = 128 + 4                # one E4M3 index key and its scale
+IDX8_BYTES_PER_QUERY = 32 * 128 + 32 * 4 + 32 * 4   # E4M3 q_idx + scales + w
 ATT_FLOP_PER_SEL = 2 * 64 * 576 + 2 * 64 * 512   # 139264
 ATT_BYTES_PER_SEL = 576 * 2                 # one gathered latent row
 ATT_BYTES_PER_QUERY = 64 * 576 * 2 + 64 * 512 * 2  # q in + out
@@ -92,6 +94,9 @@ def metric_for(wl: W.Workload):
         if wl.base == "decode":
             return f"MLA layer decode steps/s ({wl.B} seqs x {wl.ctx} ctx, top-{wl.k}; {what})", "steps/s"
         return f"MLA layer prefill tokens/s (T={wl.ctx}, top-{wl.k}; {what})", "tokens/s"
+    if wl.fp8:
+        return (f"decode steps/s with E4M3 index keys ({wl.B} seqs x {wl.ctx} ctx, top-{wl.k}; % of HBM roofline)",
+                "steps/s")
     if wl.base == "indexshare":
         return (f"IndexShare decode window steps/s ({wl.B} seqs x {wl.ctx} ctx, 1 full + {wl.steps - 1} shared "
                 f"layers, top-{wl.k})", "steps/s")
@@ -185,6 +190,15 @@ class Case:
                 c, sn = W.rotary_rows(pos)
                 self.rope.append((torch.from_numpy(c).to(device), torch.from_numpy(sn).to(device)))
             self.ik_ws = [dsa.index_key_workspace(b.total_q, device=device) for b in self.batches]
+        if wl.fp8:
+            # the cache holds E4M3 keys (quantized once, as a cache append
+            # would); the queries are quantized in every step
+            nk = wl.B * self.bt.stride
+            self.k8 = torch.empty((nk, 128), dtype=torch.uint8, device=device)
+            self.ks = torch.empty(nk, dtype=torch.float32, device=device)
+            dsa.quantize_fp8(self.bt.k_idx, self.k8, self.ks)
+            self.q8 = torch.empty((self.max_rows * 32, 128), dtype=torch.uint8, device=device)
+            self.qs = torch.empty(self.max_rows * 32, dtype=torch.float32, device=device)
         self.out = torch.empty((self.max_rows, 64, 512), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((self.max_rows, 64), dtype=torch.float32, device=device)
         self.ws = [dsa.workspace(b, wl.k, device=device) for b in self.batches]
@@ -222,6 +236,11 @@ class Case:
         for j in calls:
             q_idx, w, q = self._slices(j)
             b = self.batches[j]
+            if wl.fp8:
+                self.dsa.quantize_fp8(q_idx, self.q8, self.qs)
+                self.dsa.forward_fp8(b, self.q8, self.qs, w, self.k8, self.ks, q, self.bt.kv, wl.k,
+                                     self.bt.sm_scale, self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j])
+                continue
             self.dsa.forward(b, q_idx, w, self.bt.k_idx, q, self.bt.kv, wl.k, self.bt.sm_scale,
                              self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j])
         if wl.mla:
@@ -249,7 +268,9 @@ class Case:
             if wl.base == "indexshare":   # the shared layers repeat the attention only
                 att_flop *= wl.steps
                 att_bytes *= wl.steps
-            if wl.base in ("decode", "indexshare"):
+            if wl.fp8:
+                idx_bytes += IDX8_BYTES_PER_KEY * sum(t + 1 for t in pos) + IDX8_BYTES_PER_QUERY * len(pos)
+            elif wl.base in ("decode", "indexshare"):
                 idx_bytes += IDX_BYTES_PER_KEY * sum(t + 1 for t in pos) + IDX_BYTES_PER_QUERY * len(pos)
             else:   # one sequence: keys read once per call (they stay in L2 across query groups)
                 idx_bytes += IDX_BYTES_PER_KEY * (max(pos) + 1) + IDX_BYTES_PER_QUERY * len(pos)
@@ -276,7 +297,9 @@ class Case:
         scores = torch.empty((b.total_q, ld), dtype=torch.float32, device=self.dev)
         idx = torch.empty((b.total_q, wl.k), dtype=torch.int32, device=self.dev)
         calls = {
-            "indexer": lambda: dsa.indexer_scores(b, q_idx, w, self.bt.k_idx, scores, ld=ld, ws=self.ws[j]),
+            "indexer": (lambda: dsa.indexer_scores_fp8(b, self.q8, self.qs, w, self.k8, self.ks, scores, ld=ld,
+                                                      ws=self.ws[j])) if wl.fp8 else
+                       (lambda: dsa.indexer_scores(b, q_idx, w, self.bt.k_idx, scores, ld=ld, ws=self.ws[j])),
             "topk": lambda: dsa.topk(b, scores, wl.k, idx, ld=ld, ws=self.ws[j]),
             "sparse_mla": lambda: dsa.sparse_mla_fwd(b, q, self.bt.kv, idx, wl.k, self.bt.sm_scale,
                                                      self.out[:b.total_q], self.lse[:b.total_q], ws=self.ws[j]),
@@ -306,7 +329,9 @@ class Case:
         pos = self.positions[0]
         pairs = sum(t + 1 for t in pos)
         sel = sum(min(wl.k, t + 1) for t in pos)
-        if wl.base in ("decode", "indexshare"):
+        if wl.fp8:
+            ib = IDX8_BYTES_PER_KEY * pairs + IDX8_BYTES_PER_QUERY * len(pos)
+        elif wl.base in ("decode", "indexshare"):
             ib = IDX_BYTES_PER_KEY * pairs + IDX_BYTES_PER_QUERY * len(pos)
         else:
             ib = IDX_BYTES_PER_KEY * (max(pos) + 1) + IDX_BYTES_PER_QUERY * len(pos)
@@ -407,7 +432,7 @@ def host_sample(case: Case, n_seq: int):
     return b, rows, len(rows), f"{len(rows)} evenly spaced query rows of the {T}-token prefill"
 
 
-def oracle_path_seconds(b, rows, attention_layers: int = 1, mla=None, ik=None):
+def oracle_path_seconds(b, rows, attention_layers: int = 1, mla=None, ik=None, fp8=None):
     """The oracle's whole path on `rows`; attention_layers > 1 repeats the
     attention on the same indices (IndexShare's shared layers); mla =
     (q_nope, q_pe, w_kv_b, w_o) of those rows adds the projections around it,
@@ -419,7 +444,11 @@ def oracle_path_seconds(b, rows, attention_layers: int = 1, mla=None, ik=None):
         oracle.index_key(x, p.wk, p.gamma, p.beta, p.eps, c, sn, p.ww)
     if mla is not None:
         oracle.mla_absorb_q(mla[0], mla[1], mla[2])
-    sc = oracle.indexer_scores(b, rows)
+    if fp8 is not None:          # (k8, ks) of the cache: the queries are quantized here
+        q8, qs = oracle.quantize_fp8(b.q_idx, 128)
+        sc = oracle.indexer_scores_fp8(b, q8.reshape(-1), qs, fp8[0], fp8[1], rows)
+    else:
+        sc = oracle.indexer_scores(b, rows)
     ix = oracle.topk(b, np.nan_to_num(sc.astype(np.float32), nan=0.0), rows=rows, k=b.k)
     for _ in range(attention_layers):
         o, _ = oracle.sparse_mla(b, ix, rows=rows)
@@ -447,7 +476,12 @@ def cpu_baseline(case: Case, unit: str):
         c, sn = W.rotary_rows([case.positions[0][r] for r in rows])
         ik = (_bits(case.x[ri]), ip, c, sn)
         sample += "; with the index-key producer and the MLA projections"
-    secs = oracle_path_seconds(b, rows, mla=mla, ik=ik)
+    fp8 = None
+    if case.wl.fp8:
+        nk = b.B * b.stride
+        fp8 = (case.k8[:nk].cpu().numpy().reshape(-1), case.ks[:nk].cpu().numpy().astype(np.float64))
+        sample += "; E4M3 keys of the cache, queries quantized by the oracle"
+    secs = oracle_path_seconds(b, rows, mla=mla, ik=ik, fp8=fp8)
     # units: decode -> fraction of one step; prefill -> query rows (tokens)
     return {"value": units / secs, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": sample + f" (full path: indexer, top-k, attention; {secs:.1f} s in fp64)"}
@@ -492,8 +526,14 @@ def run_reference(args):
         ik = (W.make_hidden_np(len(rows), wl.seed + 4), W.make_index_key_params_np(wl.seed + 3), c, sn)
         sample += "; with the index-key producer and the MLA projections"
 
+    fp8 = None
+    if wl.fp8:                   # the cache's E4M3 keys, quantized once before timing
+        k8, ks = oracle.quantize_fp8(b.k_idx, 128)
+        fp8 = (k8.reshape(-1), ks)
+        sample += "; E4M3 keys, queries quantized in each step"
+
     def one_step():
-        oracle_path_seconds(b, rows, 1 + shared_layers, mla=mla, ik=ik)
+        oracle_path_seconds(b, rows, 1 + shared_layers, mla=mla, ik=ik, fp8=fp8)
 
     for _ in range(Wu):
         one_step()
@@ -691,7 +731,10 @@ def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
     if decode:                   # the new token's cache rows (a decode step appends them)
         kv3 = bt.kv.view(wl.B, bt.stride, 576)
         ki3 = bt.k_idx.view(wl.B, bt.stride, 128)
-        rows = [kv3] if wl.mla else [kv3, ki3]
+        if wl.fp8:
+            rows = [kv3, case.k8.view(wl.B, bt.stride, 128), case.ks.view(wl.B, bt.stride)]
+        else:
+            rows = [kv3] if wl.mla else [kv3, ki3]
         new_h = [r[:, wl.ctx - 1].cpu().pin_memory() for r in rows]
         stage = [[torch.empty(t.shape, dtype=t.dtype, device=comp.device) for t in new_h] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + new_h)

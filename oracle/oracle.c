@@ -513,6 +513,8 @@ void oracle_quantize_fp8(int64_t rows, int n, const uint16_t* v, uint8_t* codes,
 void oracle_indexer_scores_fp8(int B, const int32_t* q_off, const int32_t* ctx_len, int64_t stride,
                                const uint8_t* q8, const double* qs, const float* w, const uint8_t* k8,
                                const double* ks, int nrows, const int32_t* rows, double* out, int64_t ld) {
+    double val[256];                 /* every code's value, from the definition above */
+    for (int c = 0; c < 256; c++) val[c] = oracle_e4m3_decode((uint8_t)c);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int j = 0; j < nrows; j++) {
         int b;
@@ -525,7 +527,7 @@ void oracle_indexer_scores_fp8(int B, const int32_t* q_off, const int32_t* ctx_l
             for (int h = 0; h < O_HIDX; h++) {
                 const uint8_t* qr = q8 + ((int64_t)rows[j] * O_HIDX + h) * O_DIDX;
                 double dot = 0.0;
-                for (int d = 0; d < O_DIDX; d++) dot += oracle_e4m3_decode(qr[d]) * oracle_e4m3_decode(kr[d]);
+                for (int d = 0; d < O_DIDX; d++) dot += val[qr[d]] * val[kr[d]];
                 double x = qs[(int64_t)rows[j] * O_HIDX + h] * ksc * dot;
                 score += (double)w[(int64_t)rows[j] * O_HIDX + h] * (x > 0.0 ? x : 0.0);
             }

@@ -227,9 +227,14 @@ class Workload:
         return self.kind.startswith("mla_")
 
     @property
+    def fp8(self) -> bool:
+        """The index keys are cached as E4M3 codes with per-key scales."""
+        return self.kind.startswith("fp8_")
+
+    @property
     def base(self) -> str:
         """The kind of the DSA part of the step."""
-        return self.kind[4:] if self.mla else self.kind
+        return self.kind[4:] if (self.mla or self.fp8) else self.kind
 
     def describe(self) -> Dict[str, object]:
         return dataclasses.asdict(self)
@@ -253,6 +258,10 @@ WORKLOADS: Dict[str, Workload] = {
     # path: absorb the query (W_UK), then W_UV and o_proj on the output
     "mla_decode_B64_ctx32768": Workload("mla_decode_B64_ctx32768", "mla_decode", 64, 32768, 1, TOPK, "iid", 20266),
     "mla_prefill_T16384": Workload("mla_prefill_T16384", "mla_prefill", 1, 16384, 16384, TOPK, "lowrank16", 20267),
+    # the decode workload with E4M3 index keys (per-key scales) and E4M3
+    # indexer queries (per (token, head) scales), quantized each step
+    "decode_B64_ctx32768_fp8keys": Workload("decode_B64_ctx32768_fp8keys", "fp8_decode", 64, 32768, 1, TOPK, "iid",
+                                            20268),
     # long decode: 8 sequences at 202752 context, 4 decode steps
     "long_decode_B8_ctx202752": Workload("long_decode_B8_ctx202752", "decode", 8, MAX_POS, 1, TOPK, "zipf",
                                          20264, steps=4),
