@@ -210,10 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 soff[n] = (uint32_t)(sv >= 0 ? sv : 0) * (uint32_t)(kDQK * 2) + (uint32_t)(piece * 16);
             }
             for (int c = 0; c < kChunks; ++c) {
-                // chunk c of the previous block must have been consumed
-                if (jb > 0) {
+                // chunk c of the previous block must have been consumed: chunks
+                // 2i and 2i + 1 are freed together (one wait per pair)
+                if (jb > 0 && (c == kVChunks || (c & 1) == 0)) {
                     const uint32_t fb = c < kVChunks ? bar(kBarPair + c / 2) : bar(kBarO);
-                    ok = !misc[1] && mbar_wait(fb, ph ^ 1u);
+                    ok = mbar_wait(fb, ph ^ 1u);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
