@@ -289,7 +289,10 @@ cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const void* q_idx, const 
     const int32_t tiles = (bd.max_ctx + C::kBM - 1) / C::kBM;
     int tps;
     if (NQ > 1) {
-        tps = 16;
+        // query groups: long key ranges per CTA amortise its setup (TMEM,
+        // barriers, the query block) -- measured 1.10 ms at 16 tiles, 0.99 ms
+        // at 64 for a 16,384-token prefill
+        tps = 64;
     } else {
         // decode-like: spread every sequence's key stream over enough CTAs
         // for ~4 CTAs per SM in total
