@@ -87,6 +87,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Starts a prefetch into L2 of `bytes` bytes (a multiple of 16) at the
+// 16-byte aligned global address p; nothing is written to shared memory.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // L2 policy for data read exactly once: evicted first, so that it does not
 // push out data that is read again soon.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

@@ -21,7 +21,9 @@
 //               576-wide rows with 16-byte cp.async copies (8 lanes per
 //               128-byte row piece, coalesced; 8 rows per instruction pair)
 //               into nine 64-column chunks laid out 128B-swizzled; Q once
-//               by TMA
+//               by TMA.  When the caches do not stay in L2 they also start
+//               L2 prefetches of the next block's rows, so that the next
+//               gather waits on L2 rather than on HBM
 //   warp 2      TMEM owner and MMA issuer
 //   warps 3..10 softmax: thread = one gathered row and 32 of the heads (two
 //               warps per TMEM lane quarter).  The running per-head max m
@@ -30,7 +32,9 @@
 //               taken (warp max by redux.sync, then across lane quarters)
 //               and O^T rescaled in TMEM.  p = 2^(s*c - m) in fp32, written
 //               as bf16 P^T over the RoPE chunk (free once S^T is done);
-//               final normalisation and store.
+//               final normalisation into the (then free) row tile, copied
+//               out with 16-byte stores: the row's [64 heads, 512] block is
+//               contiguous in the output and in the split partials.
 // A single 144 KiB row tile fits next to Q (72 KiB); it is refilled chunk
 // by chunk as soon as the MMAs that read each chunk have completed.
 // Split-K partials (for few query rows) are merged by merge_kernel.
@@ -55,6 +59,7 @@ constexpr int kMmaWarp = kProducerWarps;                  // warp 2
 constexpr int kSoftmaxWarp0 = kMmaWarp + 1;               // warps 3..10
 constexpr int kSoftmaxThreads = 256;
 constexpr int kThreads = 32 * kSoftmaxWarp0 + kSoftmaxThreads;   // 352
+constexpr int64_t kL2PrefetchBytes = int64_t(128) << 20;  // cache bytes above which rows are prefetched
 constexpr float kRescaleLog2 = 8.0f;         // rescale O only when a max grows by > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -66,8 +71,8 @@ constexpr int kOffIdx = kOffQ + kChunks * kQChunkBytes;       // int32 [2][128]
 constexpr int kOffWmax = kOffIdx + 2 * kBlk * 4;              // float [4][64]
 constexpr int kOffM = kOffWmax + 4 * kH * 4;                  // float m_use[64]
 constexpr int kOffAlpha = kOffM + kH * 4;                     // float alpha[64]
-constexpr int kOffL = kOffAlpha + kH * 4;                     // float [4][64], then l_tot[64]
-constexpr int kOffMisc = kOffL + 5 * kH * 4;                  // u32: tmem base, abort, nblk
+constexpr int kOffL = kOffAlpha + kH * 4;                     // float [4][64], l_tot[64], 1 / l_tot[64]
+constexpr int kOffMisc = kOffL + 6 * kH * 4;                  // u32: tmem base, abort
 constexpr int kOffBar = kOffMisc + 16;
 constexpr int kBarQ = 0;
 constexpr int kBarKV = 1;                                     // [9]: chunk c landed
@@ -88,7 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_tc_kernel(const BatchDev bd, const RowRange rr, const __grid_constant__ CUtensorMap tm_q,
                          const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx, const int idx_local,
                          const int k, const int rows_per_seq, const int splits, const int per_split,
-                         const float sm_scale, uint16_t* __restrict__ out, float* __restrict__ lse,
+                         const int l2_prefetch, const float sm_scale, uint16_t* __restrict__ out,
+                         float* __restrict__ lse,
                          float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -118,16 +124,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int n) { return bar0 + 8u * (uint32_t)n; };
     const uint32_t warp = warp_id(), lane = lane_id();
 
-    // blocks of this segment: up to its last valid entry
-    if (warp == 0) {
+    // blocks of this segment: up to its last valid entry.  Every thread
+    // scans a few entries (16-byte loads when the rows are 16-byte aligned),
+    // so the scan costs one memory round trip; the per-warp maxima meet in
+    // shared memory (the block-max scratch, unused until the first block).
+    {
         int last = -1;
-#pragma unroll 8
-        for (int j = j_begin + (int)lane; j < j_end; j += 32)
-            if (__ldg(sel + j) >= 0) last = j;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-        if (lane == 0) misc[2] = last < j_begin ? 0u : (uint32_t)((last - j_begin) / kBlk + 1);
+        if ((k & 3) == 0) {
+            const int4* sel4 = reinterpret_cast<const int4*>(sel + j_begin);   // j_begin is a multiple of 128
+            for (int q = (int)threadIdx.x; q < (j_end - j_begin) >> 2; q += kThreads) {
+                const int4 v = __ldg(sel4 + q);
+                const int j = j_begin + 4 * q;
+                if (v.x >= 0) last = j;
+                if (v.y >= 0) last = j + 1;
+                if (v.z >= 0) last = j + 2;
+                if (v.w >= 0) last = j + 3;
+            }
+        } else {
+            for (int j = j_begin + (int)threadIdx.x; j < j_end; j += kThreads)
+                if (__ldg(sel + j) >= 0) last = j;
+        }
+        last = __reduce_max_sync(0xffffffffu, last);
+        if (lane == 0) reinterpret_cast<int*>(s_wmax)[warp] = last;
     }
+    if (threadIdx.x == 32 * kMmaWarp) prefetch_tmap(&tm_q);
     if (threadIdx.x == 0) {
         for (int n = 0; n < kNumBars; ++n) mbar_init(bar(n), 1);
         mbar_init(bar(kBarP), kSoftmaxThreads);
@@ -147,20 +167,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const int nblk = (int)misc[2];
+    int nblk;
+    {
+        int last = -1;
+        for (int w = 0; w < kThreads / 32; ++w) last = max(last, reinterpret_cast<const int*>(s_wmax)[w]);
+        nblk = last < j_begin ? 0 : (last - j_begin) / kBlk + 1;
+    }
+    named_bar_sync(6, kThreads);     // every thread has read the maxima before the block-max scratch is reused
     const float c2 = sm_scale * kLog2e;      // logits in log2 units
 
     if (warp < kProducerWarps) {
         // ----------------------------------------------------------- producers
-        const bool leader = threadIdx.x == 0;
-        if (leader) {
-            prefetch_tmap(&tm_q);
-            if (nblk > 0) {
-                mbar_arrive_expect_tx(bar(kBarQ), kChunks * kQChunkBytes);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_2d(sQ + c * kQChunkBytes, &tm_q, bar(kBarQ), c * 64, (int32_t)(grow * kH));
-            }
-        }
         // producer lane gl = (rq, piece): rows 8n + rq of the block, 16-byte
         // piece `piece` of each 128-byte row chunk; 8 lanes cover one row
         // chunk (coalesced) and row r % 8 == rq fixes the swizzle
@@ -172,6 +189,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jb = 0; jb < nblk; ++jb) {
             const uint32_t ph = (uint32_t)jb & 1u;
             int32_t* ib = s_idx + (jb & 1) * kBlk;
+            if (l2_prefetch && jb + 1 < nblk) {
+                // the rows of block jb + 1 (valid indices only), one
+                // 1152-byte bulk prefetch each
+                for (int u = gl; u < kBlk; u += 32 * kProducerWarps) {
+                    const int j = j_begin + (jb + 1) * kBlk + u;
+                    const int32_t sv = j < j_end ? __ldg(sel + j) : -1;
+                    if (sv >= 0 && sv <= t) prefetch_l2_bulk(kv_seq + (int64_t)sv * (kDQK * 2), kDQK * 2);
+                }
+            }
             if (warp == 0) {
                 // indices of this block: validated, -1 where invalid or past the segment
                 int32_t v[4];
@@ -235,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (misc[1]) {
             // wind down: let every copy this warp started land first
             asm volatile("cp.async.wait_all;" ::: "memory");
-            if (leader && nblk > 0) mbar_wait(bar(kBarQ), 0);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -243,7 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kH, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kH, true, true);
+            // Q by TMA (this warp is idle until it lands; the producers go
+            // straight to the first block's indices)
+            if (nblk > 0) {
+                mbar_arrive_expect_tx(bar(kBarQ), kChunks * kQChunkBytes);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_2d(sQ + c * kQChunkBytes, &tm_q, bar(kBarQ), c * 64, (int32_t)(grow * kH));
+            }
             bool ok = nblk == 0 || mbar_wait(bar(kBarQ), 0);
+            const bool q_landed = ok;
             tc_fence_after();
             for (int jb = 0; ok && jb < nblk; ++jb) {
                 const uint32_t ph = (uint32_t)jb & 1u;
@@ -290,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // every MMA this thread issued has finished once drain completes
             mma_commit(bar(kBarDrain));
             mbar_wait(bar(kBarDrain), 0);
+            if (!q_landed) mbar_wait(bar(kBarQ), 0);    // Q's copy must land before the CTA exits
         }
         __syncwarp();
     } else {
@@ -422,12 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
             if (lane == 0) s_l[lq * kH + h0 + x] = v;
         }
-        bool w = ok && (nblk == 0 || mbar_wait(bar(kBarO), ((uint32_t)nblk - 1u) & 1u));
-        w = __all_sync(0xffffffffu, w);
-        named_bar_sync(1, kSoftmaxThreads);
+        const bool got_o = ok && (nblk == 0 || mbar_wait(bar(kBarO), ((uint32_t)nblk - 1u) & 1u));
+        // agreed by every softmax thread: the staging below has a named barrier
+        const bool w = !named_bar_or(3, kSoftmaxThreads, !got_o);
         if (st < kH) {
             const float lt = s_l[st] + s_l[kH + st] + s_l[2 * kH + st] + s_l[3 * kH + st];
             s_l[4 * kH + st] = lt;
+            s_l[5 * kH + st] = lt > 0.f ? 1.f / lt : 0.f;
             const float ls = lt > 0.f ? (s_m[st] + log2f(lt)) * kLn2 : -INFINITY;
             if (splits == 1) {
                 if (lse) lse[grow * kH + st] = ls;
@@ -437,8 +472,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(1, kSoftmaxThreads);
         if (w) {
+            // every MMA has completed (PV of the last block), so the row tile
+            // is free: stage the normalised [64 heads, 512] block there
+            // (bf16 output, or fp32 split partial), then copy it out
             tc_fence_after();
-            const float* lt = s_l + 4 * kH + h0;
+            float inv[32];                                    // 1 / l of this thread's heads
+#pragma unroll
+            for (int x = 0; x < 32; x += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(s_l + 5 * kH + h0 + x);
+                inv[x] = v.x;
+                inv[x + 1] = v.y;
+                inv[x + 2] = v.z;
+                inv[x + 3] = v.w;
+            }
+            uint16_t* stage_b = reinterpret_cast<uint16_t*>(smem + kOffKV);
+            float* stage_f = reinterpret_cast<float*>(smem + kOffKV);
             for (int dv = 0; dv < 4; ++dv) {
                 const int d = dv * 128 + r;                   // output column of this thread
                 uint32_t u[32];
@@ -452,15 +500,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 32; ++x) {
                     const int h = h0 + x;
-                    const float l = lt[x];
-                    const float o = l > 0.f ? __uint_as_float(u[x]) / l : 0.f;
+                    const float o = __uint_as_float(u[x]) * inv[x];
                     if (splits == 1) {
                         const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-                        out[(grow * kH + h) * kDV + d] = *reinterpret_cast<const uint16_t*>(&ob);
+                        stage_b[h * kDV + d] = *reinterpret_cast<const uint16_t*>(&ob);
                     } else {
-                        part_o[(prow * kH + h) * kDV + d] = o;
+                        stage_f[h * kDV + d] = o;
                     }
                 }
+            }
+            named_bar_sync(1, kSoftmaxThreads);
+            {
+                const uint32_t bytes = splits == 1 ? kH * kDV * 2 : kH * kDV * 4;
+                uint4* dst = splits == 1 ? reinterpret_cast<uint4*>(out + grow * kH * kDV)
+                                         : reinterpret_cast<uint4*>(part_o + prow * kH * kDV);
+                const uint4* src = reinterpret_cast<const uint4*>(smem + kOffKV);
+                for (uint32_t o = (uint32_t)st; o < bytes / 16; o += kSoftmaxThreads) dst[o] = src[o];
             }
         }
     }
@@ -577,10 +632,13 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
     cudaError_t e =
         cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
+    // caches larger than a fraction of L2 are read from HBM: prefetch one
+    // block ahead (a cache that stays L2-resident gains nothing from it)
+    const int l2_prefetch = (int64_t)bd.B * bd.max_ctx * (kDQK * 2) > kL2PrefetchBytes ? 1 : 0;
     dim3 grid((unsigned)(rows_per_seq * splits), bd.B);
     sparse_mla_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(bd, rr, tm_q, kv, idx, idx_local ? 1 : 0, k,
-                                                                 rows_per_seq, splits, per_split, sm_scale, out,
-                                                                 lse, part_o, part_lse, status);
+                                                                 rows_per_seq, splits, per_split, l2_prefetch,
+                                                                 sm_scale, out, lse, part_o, part_lse, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1);

@@ -259,3 +259,22 @@ def test_chunked_equals_one_call():
         assert dsa.read_device_status(ws) == 0
         assert torch.equal(idx, idx_all[s])
         assert torch.equal(out.view(torch.int16), out_all[s].view(torch.int16)) and torch.equal(lse, lse_all[s])
+
+
+def test_maximum_batch_of_sequences():
+    # 65,535 sequences (the most one launch's grid takes), contexts 1..4;
+    # queries in every 997th sequence and the last two, none elsewhere, so
+    # every kernel's sequence index runs to its maximum over empty sequences;
+    # k = 2: rows with t + 1 <= k keep all positions, the others select
+    B = 65535
+    rng = np.random.default_rng(84)
+    ctx = rng.integers(1, 5, B).tolist()
+    new = [1 if (b % 997 == 0 or b >= B - 2) else 0 for b in range(B)]
+    bt = W.make_batch_np(ctx, new, k=2, seed=85)
+    st = Staged(bt)
+    out, lse, idx, sc = st.forward()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    check_scores(st, sc)
+    check_topk(st, sc, idx)
+    check_attention(st, idx, out, lse)
