@@ -21,9 +21,10 @@
 //               576-wide rows with 16-byte cp.async copies (8 lanes per
 //               128-byte row piece, coalesced; 8 rows per instruction pair)
 //               into nine 64-column chunks laid out 128B-swizzled; Q once
-//               by TMA.  When the caches do not stay in L2 they also start
-//               L2 prefetches of the next block's rows, so that the next
-//               gather waits on L2 rather than on HBM
+//               by TMA.  When the caches do not stay in L2, the rows of the
+//               next block are prefetched into L2 (the first block's during
+//               the index scan), so that a gather waits on L2 rather than on
+//               HBM
 //   warp 2      TMEM owner and MMA issuer
 //   warps 3..10 softmax: thread = one gathered row and 32 of the heads (two
 //               warps per TMEM lane quarter).  The running per-head max m
@@ -60,6 +61,7 @@ constexpr int kSoftmaxWarp0 = kMmaWarp + 1;               // warps 3..10
 constexpr int kSoftmaxThreads = 256;
 constexpr int kThreads = 32 * kSoftmaxWarp0 + kSoftmaxThreads;   // 352
 constexpr int64_t kL2PrefetchBytes = int64_t(128) << 20;  // cache bytes above which rows are prefetched
+constexpr int kPrefetchAhead = 1;                         // blocks prefetched ahead of the gather
 constexpr float kRescaleLog2 = 8.0f;         // rescale O only when a max grows by > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -128,6 +130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scans a few entries (16-byte loads when the rows are 16-byte aligned),
     // so the scan costs one memory round trip; the per-warp maxima meet in
     // shared memory (the block-max scratch, unused until the first block).
+    // With L2 prefetching on, the rows of the first kPrefetchAhead blocks
+    // are prefetched as their indices are seen.
+    const uint8_t* kv_seq = reinterpret_cast<const uint8_t*>(kv) + (int64_t)b * bd.stride * (kDQK * 2);
+    auto prefetch_row = [&](int j, int32_t sv) {
+        if (l2_prefetch && j < j_begin + kPrefetchAhead * kBlk && sv >= 0 && sv <= t)
+            prefetch_l2_bulk(kv_seq + (int64_t)sv * (kDQK * 2), kDQK * 2);
+    };
     {
         int last = -1;
         if ((k & 3) == 0) {
@@ -139,10 +148,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (v.y >= 0) last = j + 1;
                 if (v.z >= 0) last = j + 2;
                 if (v.w >= 0) last = j + 3;
+                prefetch_row(j, v.x);
+                prefetch_row(j + 1, v.y);
+                prefetch_row(j + 2, v.z);
+                prefetch_row(j + 3, v.w);
             }
         } else {
-            for (int j = j_begin + (int)threadIdx.x; j < j_end; j += kThreads)
-                if (__ldg(sel + j) >= 0) last = j;
+            for (int j = j_begin + (int)threadIdx.x; j < j_end; j += kThreads) {
+                const int32_t sv = __ldg(sel + j);
+                if (sv >= 0) last = j;
+                prefetch_row(j, sv);
+            }
         }
         last = __reduce_max_sync(0xffffffffu, last);
         if (lane == 0) reinterpret_cast<int*>(s_wmax)[warp] = last;
@@ -184,16 +200,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gl = (int)threadIdx.x;
         const int rq = gl >> 3, piece = gl & 7;
         const uint32_t dpat = (uint32_t)(rq * 128 + ((piece ^ rq) << 4));
-        const uint8_t* kv_seq = reinterpret_cast<const uint8_t*>(kv) + (int64_t)b * bd.stride * (kDQK * 2);
         bool ok = true;
         for (int jb = 0; jb < nblk; ++jb) {
             const uint32_t ph = (uint32_t)jb & 1u;
             int32_t* ib = s_idx + (jb & 1) * kBlk;
-            if (l2_prefetch && jb + 1 < nblk) {
-                // the rows of block jb + 1 (valid indices only), one
-                // 1152-byte bulk prefetch each
+            if (l2_prefetch && jb + kPrefetchAhead < nblk) {
+                // the rows of block jb + kPrefetchAhead (valid indices only),
+                // one 1152-byte bulk prefetch each
                 for (int u = gl; u < kBlk; u += 32 * kProducerWarps) {
-                    const int j = j_begin + (jb + 1) * kBlk + u;
+                    const int j = j_begin + (jb + kPrefetchAhead) * kBlk + u;
                     const int32_t sv = j < j_end ? __ldg(sel + j) : -1;
                     if (sv >= 0 && sv <= t) prefetch_l2_bulk(kv_seq + (int64_t)sv * (kDQK * 2), kDQK * 2);
                 }
@@ -212,9 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[u] = sv;
                 }
                 // buffer jb & 1 was last read by the softmax of block jb - 2,
-                // which finished before PV(jb - 1) started
-                ok = jb == 0 || (!misc[1] && mbar_wait(bar(kBarPair), ph ^ 1u));
-                ok = __all_sync(0xffffffffu, ok);
+                // which finished before PV(jb - 2) started; these warps have
+                // already waited for PV(jb - 2) to complete (before refilling
+                // chunk 8 in block jb - 1), so the buffer is free and the
+                // block's indices and row offsets are ready before PV(jb - 1)
+                ok = __all_sync(0xffffffffu, !misc[1]);
                 if (ok) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) ib[u * 32 + lane] = v[u];
