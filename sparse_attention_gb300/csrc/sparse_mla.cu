@@ -38,7 +38,11 @@
 //               contiguous in the output and in the split partials.
 // A single 144 KiB row tile fits next to Q (72 KiB); it is refilled chunk
 // by chunk as soon as the MMAs that read each chunk have completed.
-// Split-K partials (for few query rows) are merged by merge_kernel.
+// Split-K partials (for few query rows): with 2 or 4 splits the CTAs of a
+// row form a cluster and merge through distributed shared memory (each CTA
+// combines every split's staged rows for a quarter or half of the heads);
+// more splits write fp32 partials that merge_kernel combines.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -46,6 +50,8 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 namespace {
@@ -62,6 +68,7 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kThreads = 32 * kSoftmaxWarp0 + kSoftmaxThreads;   // 352
 constexpr int64_t kL2PrefetchBytes = int64_t(128) << 20;  // cache bytes above which rows are prefetched
 constexpr int kPrefetchAhead = 1;                         // blocks prefetched ahead of the gather
+constexpr int kMaxClusterMerge = 4;                       // most splits merged inside a cluster
 constexpr float kRescaleLog2 = 8.0f;         // rescale O only when a max grows by > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -73,8 +80,8 @@ constexpr int kOffIdx = kOffQ + kChunks * kQChunkBytes;       // int32 [2][128]
 constexpr int kOffWmax = kOffIdx + 2 * kBlk * 4;              // float [4][64]
 constexpr int kOffM = kOffWmax + 4 * kH * 4;                  // float m_use[64]
 constexpr int kOffAlpha = kOffM + kH * 4;                     // float alpha[64]
-constexpr int kOffL = kOffAlpha + kH * 4;                     // float [4][64], l_tot[64], 1 / l_tot[64]
-constexpr int kOffMisc = kOffL + 6 * kH * 4;                  // u32: tmem base, abort
+constexpr int kOffL = kOffAlpha + kH * 4;                     // float [4][64], l_tot[64], 1 / l_tot[64], lse[64]
+constexpr int kOffMisc = kOffL + 7 * kH * 4;                  // u32: tmem base, abort, rows staged
 constexpr int kOffBar = kOffMisc + 16;
 constexpr int kBarQ = 0;
 constexpr int kBarKV = 1;                                     // [9]: chunk c landed
@@ -95,7 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_tc_kernel(const BatchDev bd, const RowRange rr, const __grid_constant__ CUtensorMap tm_q,
                          const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx, const int idx_local,
                          const int k, const int rows_per_seq, const int splits, const int per_split,
-                         const int l2_prefetch, const float sm_scale, uint16_t* __restrict__ out,
+                         const int l2_prefetch, const int cluster_merge, const float sm_scale,
+                         uint16_t* __restrict__ out,
                          float* __restrict__ lse,
                          float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status) {
     extern __shared__ uint8_t smem_raw[];
@@ -171,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kBarIdx + 1), 32);
         for (int c = 0; c < kChunks; ++c) mbar_init(bar(kBarKV + c), 32 * kProducerWarps);
         misc[1] = 0;
+        misc[2] = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -483,6 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float ls = lt > 0.f ? (s_m[st] + log2f(lt)) * kLn2 : -INFINITY;
             if (splits == 1) {
                 if (lse) lse[grow * kH + st] = ls;
+            } else if (cluster_merge) {
+                s_l[6 * kH + st] = ls;
             } else {
                 part_lse[prow * kH + st] = ls;
             }
@@ -527,7 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             named_bar_sync(1, kSoftmaxThreads);
-            {
+            if (cluster_merge) {
+                if (st == 0) misc[2] = 1u;                    // staged: the cluster may read it
+            } else {
                 const uint32_t bytes = splits == 1 ? kH * kDV * 2 : kH * kDV * 4;
                 uint4* dst = splits == 1 ? reinterpret_cast<uint4*>(out + grow * kH * kDV)
                                          : reinterpret_cast<uint4*>(part_o + prow * kH * kDV);
@@ -535,6 +548,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (uint32_t o = (uint32_t)st; o < bytes / 16; o += kSoftmaxThreads) dst[o] = src[o];
             }
         }
+    }
+
+    if (cluster_merge) {
+        // The row's splits are the CTAs of this cluster, rank = split.  Each
+        // merges heads h = rank (mod splits) from every split's staged rows:
+        // out = sum_s exp(lse_s - m) o_s / sum_s exp(lse_s - m), m = max lse_s
+        // (the arithmetic of merge_kernel, in the same order).
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();                                       // every split has staged (or failed)
+        if (warp >= kSoftmaxWarp0) {
+            const int st = (int)threadIdx.x - 32 * kSoftmaxWarp0;
+            const uint32_t* flag = reinterpret_cast<const uint32_t*>(smem + kOffMisc) + 2;
+            bool all = true;
+            for (int s2 = 0; s2 < splits; ++s2) all = all && *cluster.map_shared_rank(flag, (unsigned)s2) != 0u;
+            if (all) {
+                const float* r_lse[kMaxClusterMerge];
+                const float4* r_o[kMaxClusterMerge];
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
+                    const unsigned rk = (unsigned)min(s2, splits - 1);
+                    r_lse[s2] = cluster.map_shared_rank(s_l + 6 * kH, rk);
+                    r_o[s2] = cluster.map_shared_rank(reinterpret_cast<const float4*>(smem + kOffKV), rk);
+                }
+                const int hs = kH / splits;
+                for (int item = st; item < hs * (kDV / 4); item += kSoftmaxThreads) {
+                    const int h = sp + splits * (item / (kDV / 4));
+                    const int d4 = item % (kDV / 4);
+                    float ls[kMaxClusterMerge];
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
+                        ls[s2] = s2 < splits ? r_lse[s2][h] : -INFINITY;
+                        mx = fmaxf(mx, ls[s2]);
+                    }
+                    float wsum = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (mx > -INFINITY) {
+#pragma unroll
+                        for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
+                            if (s2 >= splits || ls[s2] == -INFINITY) continue;
+                            const float wgt = expf(ls[s2] - mx);
+                            wsum += wgt;
+                            const float4 v = r_o[s2][h * (kDV / 4) + d4];
+                            acc.x = fmaf(wgt, v.x, acc.x);
+                            acc.y = fmaf(wgt, v.y, acc.y);
+                            acc.z = fmaf(wgt, v.z, acc.z);
+                            acc.w = fmaf(wgt, v.w, acc.w);
+                        }
+                    }
+                    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+                    uint2 pk;
+                    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2*>(out + (grow * kH + h) * kDV + 4 * d4) = pk;
+                    if (lse && d4 == 0) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+                }
+            }
+        }
+        cluster.sync();                                       // no partial is read after its CTA exits
     }
 
     tc_fence_before();
@@ -616,6 +688,10 @@ int choose_splits(int64_t rows, int k) {
     return best;
 }
 
+// Splits merged inside a cluster: the count divides the heads and is small
+// enough that a cluster of that many one-SM CTAs always fits in a GPC.
+bool merge_in_cluster(int splits) { return splits > 1 && splits <= kMaxClusterMerge && kH % splits == 0; }
+
 }  // namespace
 
 // The split count depends only on the batch bounds, never on how many rows
@@ -623,7 +699,7 @@ int choose_splits(int64_t rows, int k) {
 size_t sparse_mla_scratch_bytes(const BatchDev& bd, int64_t rows_per_seq, int k) {
     const int64_t rows = rows_per_seq * bd.B;
     const int splits = choose_splits((int64_t)bd.B * bd.max_q, k);
-    if (splits <= 1) return 0;
+    if (splits <= 1 || merge_in_cluster(splits)) return 0;
     return (size_t)rows * splits * kH * (kDV + 1) * sizeof(float);
 }
 
@@ -636,9 +712,10 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
     const int64_t rows = (int64_t)rows_per_seq * bd.B;
     const int splits = choose_splits((int64_t)bd.B * bd.max_q, k);
     const int per_split = ((k + splits - 1) / splits + kBlk - 1) / kBlk * kBlk;
+    const bool cluster_merge = merge_in_cluster(splits);
     float* part_o = nullptr;
     float* part_lse = nullptr;
-    if (splits > 1) {
+    if (splits > 1 && !cluster_merge) {
         const size_t need = sparse_mla_scratch_bytes(bd, rows_per_seq, k);
         if (!scratch || scratch_bytes < need) return cudaErrorInvalidValue;
         part_o = static_cast<float*>(scratch);
@@ -652,14 +729,24 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
     // caches larger than a fraction of L2 are read from HBM: prefetch one
     // block ahead (a cache that stays L2-resident gains nothing from it)
     const int l2_prefetch = (int64_t)bd.B * bd.max_ctx * (kDQK * 2) > kL2PrefetchBytes ? 1 : 0;
-    dim3 grid((unsigned)(rows_per_seq * splits), bd.B);
-    sparse_mla_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(bd, rr, tm_q, kv, idx, idx_local ? 1 : 0, k,
-                                                                 rows_per_seq, splits, per_split, l2_prefetch,
-                                                                 sm_scale, out, lse, part_o, part_lse, status);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows_per_seq * splits), (unsigned)bd.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster_merge ? (unsigned)splits : 1u;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, bd, rr, tm_q, kv, idx, idx_local ? 1 : 0, k, rows_per_seq,
+                           splits, per_split, l2_prefetch, cluster_merge ? 1 : 0, sm_scale, out, lse, part_o,
+                           part_lse, status);
     if (e != cudaSuccess) return e;
     count_launches(1);
-    if (splits == 1) return e;
+    if (splits == 1 || cluster_merge) return e;
     merge_kernel<<<dim3(rows_per_seq * 8, bd.B), 256, 0, stream>>>(bd, rr, rows_per_seq, splits, part_o,
                                                                   part_lse, out, lse, status);
     e = cudaGetLastError();

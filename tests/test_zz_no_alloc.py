@@ -64,11 +64,12 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
 
 
 def test_noalloc_rejects_partials_beyond_the_static_array(lib):
-    # 1140 query rows at k = 2047 split each row in two: 2280 partials of
-    # 131,328 B do not fit in 32 MiB.  Every buffer is real and sized for the
-    # batch (all indices -1), so the call could not touch memory it does not
-    # own even if it launched; it must refuse before launching.
-    T, ctx, k = 1140, 4096, 2047
+    # 100 query rows at k = 2047 split each row in three (merged by a second
+    # kernel, not in a cluster): 300 partials of 131,328 B do not fit in
+    # 32 MiB.  Every buffer is real and sized for the batch (all indices -1),
+    # so the call could not touch memory it does not own even if it
+    # launched; it must refuse before launching.
+    T, ctx, k = 100, 4096, 2047
     b = dsa.make_batch([0, T], [ctx], T, ctx, ctx)
     q = torch.zeros((T, 64, 576), dtype=torch.bfloat16, device="cuda")
     kv = torch.zeros((ctx, 576), dtype=torch.bfloat16, device="cuda")
