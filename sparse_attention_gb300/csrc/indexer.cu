@@ -83,7 +83,9 @@ __global__ void __launch_bounds__(IdxCfg<NQ, kFp8>::kThreads, 1)
     const int b = blockIdx.z;
     SeqInfo sq;
     if (!load_seq(bd, b, status, sq)) return;
-    const int32_t qlo = rr.i0 + (int32_t)blockIdx.y * NQ;           // local query indices [qlo, qhi)
+    // query groups in reverse: the longest causal key ranges start first,
+    // which shortens the launch's tail (16,384-token prefill: 0.99 -> 0.95 ms)
+    const int32_t qlo = rr.i0 + (int32_t)(gridDim.y - 1 - blockIdx.y) * NQ;   // local query indices [qlo, qhi)
     const int32_t qhi = min(min(qlo + NQ, rr.i1), sq.nq);
     if (qlo >= qhi) return;
     const int32_t pos0 = sq.ctx - sq.nq;                             // position of local query 0

@@ -87,7 +87,7 @@ constexpr int kBarQ = 0;
 constexpr int kBarKV = 1;                                     // [9]: chunk c landed
 constexpr int kBarPair = kBarKV + kChunks;                    // [4]: chunks 2i, 2i+1 consumed
 constexpr int kBarS = kBarPair + 4;                           // S^T ready
-constexpr int kBarP = kBarS + 1;                              // P^T written (128 arrivals)
+constexpr int kBarP = kBarS + 1;                              // P^T written (one arrival per softmax warp)
 constexpr int kBarO = kBarP + 1;                              // PV of a block done (chunk 8 free)
 constexpr int kBarIdx = kBarO + 1;                            // [2]: indices of a block published
 constexpr int kBarDrain = kBarIdx + 2;
@@ -174,9 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 32 * kMmaWarp) prefetch_tmap(&tm_q);
     if (threadIdx.x == 0) {
         for (int n = 0; n < kNumBars; ++n) mbar_init(bar(n), 1);
-        mbar_init(bar(kBarP), kSoftmaxThreads);
-        mbar_init(bar(kBarIdx), 32);
-        mbar_init(bar(kBarIdx + 1), 32);
+        mbar_init(bar(kBarP), kSoftmaxThreads / 32);
+        mbar_init(bar(kBarIdx), 1);
+        mbar_init(bar(kBarIdx + 1), 1);
         for (int c = 0; c < kChunks; ++c) mbar_init(bar(kBarKV + c), 32 * kProducerWarps);
         misc[1] = 0;
         misc[2] = 0;
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) ib[u * 32 + lane] = v[u];
                     __syncwarp();
-                    mbar_arrive(bar(kBarIdx + (jb & 1)));
+                    if (lane == 0) mbar_arrive(bar(kBarIdx + (jb & 1)));
                 } else {
                     misc[1] = 1;
                 }
@@ -465,9 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c8 = (h0 >> 3) + e4;
                 *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = pk;
             }
+            // one arrival per warp once all its lanes' P^T writes are fenced
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(kBarP));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarP));
         }
         if (!ok) {
             latch_status(status, DSA_ERR_TIMEOUT);
