@@ -213,6 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jb = 0; jb < nblk; ++jb) {
             const uint32_t ph = (uint32_t)jb & 1u;
             int32_t* ib = s_idx + (jb & 1) * kBlk;
+            // this block's indices (warp 0) are loaded before the prefetch
+            // below, so that the two round trips overlap
+            int32_t v[4];
+            if (warp == 0) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = j_begin + jb * kBlk + u * 32 + (int)lane;
+                    v[u] = (j < j_end) ? __ldg(sel + j) : -1;
+                }
+            }
             if (l2_prefetch && jb + kPrefetchAhead < nblk) {
                 // the rows of block jb + kPrefetchAhead (valid indices only),
                 // one 1152-byte bulk prefetch each
@@ -224,16 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (warp == 0) {
                 // indices of this block: validated, -1 where invalid or past the segment
-                int32_t v[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int j = j_begin + jb * kBlk + u * 32 + (int)lane;
-                    int32_t sv = (j < j_end) ? __ldg(sel + j) : -1;
-                    if (sv < -1 || sv > t) {
+                    if (v[u] < -1 || v[u] > t) {
                         latch_status(status, DSA_ERR_BAD_INDEX);
-                        sv = -1;
+                        v[u] = -1;
                     }
-                    v[u] = sv;
                 }
                 // buffer jb & 1 was last read by the softmax of block jb - 2,
                 // which finished before PV(jb - 2) started; these warps have
