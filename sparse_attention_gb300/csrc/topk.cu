@@ -45,7 +45,7 @@ namespace {
 // Threads per CTA: 1024 when a launch has fewer rows than SMs (one CTA per
 // SM, more warps to hide latency), else 512 (two CTAs per SM).
 constexpr int kBins = 2048;
-constexpr int kSample = 1024;
+constexpr int kSample = 512;
 constexpr int kRegion = 512;                 // candidate slots per warp
 constexpr int kPrefetch = 8;                 // 16-byte loads in flight per lane (32 keys)
 static_assert(kPrefetch <= 8, "a lane's candidate flags fill one 32-bit word, its counts one 64-bit word");
