@@ -72,14 +72,24 @@ __global__ void __launch_bounds__(256)
     }
     const int64_t t = (int64_t)sq.ctx - sq.nq + i;
 
-    // k: the four dims of this lane, splits summed in order
-    float v[4];
+    // k: the four dims of this lane, splits summed in order (loads of four
+    // splits in flight at a time)
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    int s = 0;
+    for (; s + 4 <= sk; s += 4) {
+        float t4[4][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float acc = 0.f;
-        for (int s = 0; s < sk; ++s) acc += part_k[((int64_t)s * bd.total_q + r) * kDIdx + lane + 32 * j];
-        v[j] = acc;
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) t4[u][j] = part_k[((int64_t)(s + u) * bd.total_q + r) * kDIdx + lane + 32 * j];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] += t4[u][j];
     }
+    for (; s < sk; ++s)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] += part_k[((int64_t)s * bd.total_q + r) * kDIdx + lane + 32 * j];
     float sum = (v[0] + v[1]) + (v[2] + v[3]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -108,9 +118,17 @@ __global__ void __launch_bounds__(256)
         const __nv_bfloat16 bv = __float2bfloat16_rn(outv[j]);
         krow[lane + 32 * j] = *reinterpret_cast<const uint16_t*>(&bv);
     }
-    // w: one head per lane
+    // w: one head per lane (eight splits' loads in flight at a time)
     float acc = 0.f;
-    for (int s = 0; s < sw; ++s) acc += part_w[((int64_t)s * bd.total_q + r) * kHIdx + lane];
+    int s2 = 0;
+    for (; s2 + 8 <= sw; s2 += 8) {
+        float t8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) t8[u] = part_w[((int64_t)(s2 + u) * bd.total_q + r) * kHIdx + lane];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc += t8[u];
+    }
+    for (; s2 < sw; ++s2) acc += part_w[((int64_t)s2 * bd.total_q + r) * kHIdx + lane];
     w_out[r * kHIdx + lane] = acc * rsqrtf((float)kHIdx);
 }
 

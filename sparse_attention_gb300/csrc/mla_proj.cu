@@ -305,12 +305,14 @@ __global__ void copy_rope_kernel(int64_t rows, const uint4* __restrict__ q_pe, u
 }
 
 // K splits of a GEMM whose output tiles fill few SMs: enough CTAs for about
-// one wave, each with at least 4 k-tiles.  Depends only on the shape.
+// one wave, each with at least 8 k-tiles (fewer made the split-sum pass
+// cost more than the extra CTAs saved: 64-token W_UV is not split, 64-token
+// index-key products split 12 ways).  Depends only on the shape.
 int choose_k_splits(int32_t M, int32_t N, int32_t K, int32_t batches) {
     const int64_t tiles = (int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN) * batches;
     const int32_t nk = K / kBK;
     if (tiles == 0 || tiles * 2 > kNumSMs) return 1;
-    return (int)std::max<int64_t>(1, std::min<int64_t>(nk / 4, kNumSMs / tiles));
+    return (int)std::max<int64_t>(1, std::min<int64_t>(nk / 8, kNumSMs / tiles));
 }
 
 template <bool kBMn>
