@@ -127,12 +127,20 @@ __device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSme
             for (int x = 0; x < kBinsPerThread; ++x) c[x] = S.hist[kBinsPerThread * tid + x];
         } else {
             cluster.sync();
+            // every rank's counts loaded at once (predicated loads, one
+            // distributed-shared-memory round trip), then summed in rank order
+            uint32_t rc[kMaxCluster][kBinsPerThread];
 #pragma unroll
-            for (int x = 0; x < kBinsPerThread; ++x) c[x] = 0u;
-            for (int r = 0; r < nranks; ++r) {
-                const uint32_t* h = cluster.map_shared_rank(S.hist, r);
+            for (int r = 0; r < kMaxCluster; ++r) {
+                const uint32_t* h = cluster.map_shared_rank(S.hist, (unsigned)min(r, nranks - 1));
 #pragma unroll
-                for (int x = 0; x < kBinsPerThread; ++x) c[x] += h[kBinsPerThread * tid + x];
+                for (int x = 0; x < kBinsPerThread; ++x) rc[r][x] = r < nranks ? h[kBinsPerThread * tid + x] : 0u;
+            }
+#pragma unroll
+            for (int x = 0; x < kBinsPerThread; ++x) {
+                c[x] = 0u;
+#pragma unroll
+                for (int r = 0; r < kMaxCluster; ++r) c[x] += rc[r][x];
             }
             cluster.sync();                        // every remote read done before any bin is cleared
         }
