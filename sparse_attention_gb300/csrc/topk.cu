@@ -252,12 +252,20 @@ __device__ __forceinline__ int varying_bits(uint32_t lo, uint32_t hi) {
 template <int NT>
 __device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, int crank, TopkSmem<NT>& S,
                                                uint32_t& gt0, uint32_t& eq0) {
+    // every lower rank's counts loaded at once (predicated), then summed
+    uint32_t g[kMaxCluster], e[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+        const TopkSmem<NT>* o = cluster.map_shared_rank(&S, (unsigned)min(r, max(crank - 1, 0)));
+        g[r] = r < crank ? o->cta_gt : 0u;
+        e[r] = r < crank ? o->cta_eq : 0u;
+    }
     gt0 = 0u;
     eq0 = 0u;
-    for (int r = 0; r < crank; ++r) {
-        const TopkSmem<NT>* o = cluster.map_shared_rank(&S, r);
-        gt0 += o->cta_gt;
-        eq0 += o->cta_eq;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+        gt0 += g[r];
+        eq0 += e[r];
     }
 }
 
@@ -425,11 +433,26 @@ __global__ void __launch_bounds__(NT, NT <= 512 ? 2 : 1)
     }
     sync_row();
     uint32_t all_cand = 0u, any_overflow = 0u, all_max = 0u;
-    for (int q = 0; q < csize; ++q) {
-        const TopkSmem<NT>* o = csize == 1 ? &S : cluster.map_shared_rank(&S, q);
-        all_cand += o->cta_cand;
-        any_overflow |= o->cta_overflow;
-        all_max = max(all_max, o->cta_max);
+    if (csize == 1) {
+        all_cand = S.cta_cand;
+        any_overflow = S.cta_overflow;
+        all_max = S.cta_max;
+    } else {
+        // every rank's counts loaded at once (predicated), then combined
+        uint32_t cc[kMaxCluster], co[kMaxCluster], cm[kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q) {
+            const TopkSmem<NT>* o = cluster.map_shared_rank(&S, (unsigned)min(q, csize - 1));
+            cc[q] = q < csize ? o->cta_cand : 0u;
+            co[q] = q < csize ? o->cta_overflow : 0u;
+            cm[q] = q < csize ? o->cta_max : 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q) {
+            all_cand += cc[q];
+            any_overflow |= co[q];
+            all_max = max(all_max, cm[q]);
+        }
     }
     const bool use_candidates = !any_overflow && all_cand >= (uint32_t)k;
 
