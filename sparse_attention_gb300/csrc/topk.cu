@@ -193,17 +193,20 @@ __device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSme
             };
             if (tid < 64 * nranks) {
                 const int r = tid >> 6, e = tid & 63;
-                const TopkSmem<NT>* o = rank_smem(r);
-                if ((uint32_t)e < min(o->small_n, 64u)) {
-                    uint32_t off = 0u;
-                    for (int r2 = 0; r2 < r; ++r2) off += min(rank_smem(r2)->small_n, 64u);
-                    if (off + (uint32_t)e < 64u) S.small_all[off + e] = o->small[e];
+                // every rank's list length, loaded at once (predicated)
+                uint32_t len[kMaxCluster];
+#pragma unroll
+                for (int r2 = 0; r2 < kMaxCluster; ++r2)
+                    len[r2] = r2 < nranks ? min(rank_smem(min(r2, nranks - 1))->small_n, 64u) : 0u;
+                uint32_t off = 0u, mine = 0u, tot = 0u;
+#pragma unroll
+                for (int r2 = 0; r2 < kMaxCluster; ++r2) {
+                    off += r2 < r ? len[r2] : 0u;
+                    mine = r2 == r ? len[r2] : mine;
+                    tot += len[r2];
                 }
-            }
-            if (tid == 0) {
-                uint32_t tot = 0u;
-                for (int r2 = 0; r2 < nranks; ++r2) tot += min(rank_smem(r2)->small_n, 64u);
-                S.small_all_n = min(tot, 64u);
+                if ((uint32_t)e < mine && off + (uint32_t)e < 64u) S.small_all[off + e] = rank_smem(r)->small[e];
+                if (tid == 0) S.small_all_n = min(tot, 64u);
             }
             __syncthreads();
             // thread t ranks key t / 8 against keys 8 (t % 8) .. 8 (t % 8) + 7;
