@@ -80,7 +80,8 @@ constexpr int kOffIdx = kOffQ + kChunks * kQChunkBytes;       // int32 [2][128]
 constexpr int kOffWmax = kOffIdx + 2 * kBlk * 4;              // float [4][64]
 constexpr int kOffM = kOffWmax + 4 * kH * 4;                  // float m_use[64]
 constexpr int kOffAlpha = kOffM + kH * 4;                     // float alpha[64]
-constexpr int kOffL = kOffAlpha + kH * 4;                     // float [4][64], l_tot[64], 1 / l_tot[64], lse[64]
+constexpr int kOffThr = kOffAlpha + kH * 4;                   // float thr[64]: the vote's bound in raw score units
+constexpr int kOffL = kOffThr + kH * 4;                       // float [4][64], l_tot[64], 1 / l_tot[64], lse[64]
 constexpr int kOffMisc = kOffL + 7 * kH * 4;                  // u32: tmem base, abort, rows staged
 constexpr int kOffBar = kOffMisc + 16;
 constexpr int kBarQ = 0;
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* s_wmax = reinterpret_cast<float*>(smem + kOffWmax);
     float* s_m = reinterpret_cast<float*>(smem + kOffM);
     float* s_alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+    float* s_thr = reinterpret_cast<float*>(smem + kOffThr);
     float* s_l = reinterpret_cast<float*>(smem + kOffL);
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
     const uint32_t bar0 = smem_u32(smem + kOffBar);
@@ -186,8 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
         tmem_relinquish();
     }
-    if (threadIdx.x >= 32 * kSoftmaxWarp0 && threadIdx.x < 32 * kSoftmaxWarp0 + kH)
+    if (threadIdx.x >= 32 * kSoftmaxWarp0 && threadIdx.x < 32 * kSoftmaxWarp0 + kH) {
         s_m[threadIdx.x - 32 * kSoftmaxWarp0] = -INFINITY;
+        s_thr[threadIdx.x - 32 * kSoftmaxWarp0] = -INFINITY;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -390,15 +394,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 32; ++x) s[x] = valid ? __uint_as_float(u[x]) : -INFINITY;
             }
-            // the running max moves only when a score exceeds it by 2^8
+            // the running max moves only when a score exceeds it by 2^8; the
+            // vote compares raw scores with (m + 8) / c2 per head (a trigger
+            // only: the exact block max below decides whether m moves)
             bool exceed = false;
 #pragma unroll
             for (int x = 0; x < 32; x += 4) {
-                const float4 mv = *reinterpret_cast<const float4*>(s_m + h0 + x);
-                exceed |= s[x] * c2 > mv.x + kRescaleLog2;
-                exceed |= s[x + 1] * c2 > mv.y + kRescaleLog2;
-                exceed |= s[x + 2] * c2 > mv.z + kRescaleLog2;
-                exceed |= s[x + 3] * c2 > mv.w + kRescaleLog2;
+                const float4 tv = *reinterpret_cast<const float4*>(s_thr + h0 + x);
+                exceed |= s[x] > tv.x;
+                exceed |= s[x + 1] > tv.y;
+                exceed |= s[x + 2] > tv.z;
+                exceed |= s[x + 3] > tv.w;
             }
             if (named_bar_or(2, kSoftmaxThreads, exceed)) {
                 // exact per-head block max: warp max, then across lane quarters
@@ -418,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (mb > -INFINITY && (mold == -INFINITY || mnew > mold + kRescaleLog2)) {
                         alpha = exp2f(mold - mnew);          // 0 when nothing was seen yet
                         s_m[st] = mnew;
+                        s_thr[st] = (mnew + kRescaleLog2) / c2;
                         need = true;
                     }
                     s_alpha[st] = alpha;
