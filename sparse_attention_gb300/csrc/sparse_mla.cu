@@ -20,12 +20,11 @@
 //   warps 0, 1  producers: validate the block's indices and gather the
 //               576-wide rows with 16-byte cp.async copies (8 lanes per
 //               128-byte row piece, coalesced; 8 rows per instruction pair)
-//               into nine 64-column chunks laid out 128B-swizzled; Q once
-//               by TMA.  When the caches do not stay in L2, the rows of the
-//               next block are prefetched into L2 (the first block's during
-//               the index scan), so that a gather waits on L2 rather than on
-//               HBM
-//   warp 2      TMEM owner and MMA issuer
+//               into nine 64-column chunks laid out 128B-swizzled.  When
+//               the caches do not stay in L2, the rows of the next block are
+//               prefetched into L2 (the first block's during the index
+//               scan), so that a gather waits on L2 rather than on HBM
+//   warp 2      TMEM owner; loads Q once by TMA; MMA issuer
 //   warps 3..10 softmax: thread = one gathered row and 32 of the heads (two
 //               warps per TMEM lane quarter).  The running per-head max m
 //               only moves when some score exceeds it by more than 2^8 (a
