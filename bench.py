@@ -499,17 +499,19 @@ def run_reference(args):
     K, Wu = default_steps(wl)
     K = args.steps if args.steps is not None else K
     Wu = args.warmup if args.warmup is not None else Wu
-    # one bounded sample per step, drawn with the numpy recipe
+    # one bounded sample per step, drawn with the numpy recipe: one query
+    # row per host thread (the oracle runs its rows in parallel)
     shared_layers = wl.steps - 1 if wl.base == "indexshare" else 0
+    threads = max(1, oracle.num_threads())
     if wl.base in ("decode", "indexshare"):
-        ns = 1
+        ns = min(wl.B, threads)
         b = W.make_batch_np([wl.ctx] * ns, [1] * ns, wl.k, wl.seed, key_kind=wl.key_kind)
         rows = list(range(ns))
         frac = ns / wl.B
         sample = f"{ns} of {wl.B} sequences of one decode step per timed step"
     else:
         T = wl.ctx
-        nq = 4
+        nq = threads
         b = W.make_batch_np([T], [T], wl.k, wl.seed, key_kind=wl.key_kind) if T <= 16384 else None
         if b is None:
             print(json.dumps({"impl": "reference", "unavailable": "oracle sample of this workload exceeds host memory"}))
