@@ -464,7 +464,7 @@ def _bits(t):
 
 def cpu_baseline(case: Case, unit: str):
     import oracle
-    n = 24 if case.wl.base == "decode" else 48
+    n = 64 if case.wl.base == "decode" else 48      # decode: every sequence of the step (B <= 64)
     b, rows, units, sample = host_sample(case, n)
     mla = ik = None
     if case.wl.mla:
