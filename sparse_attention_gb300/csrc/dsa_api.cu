@@ -22,6 +22,17 @@ namespace {
 // 60.6 ms and 53.0 ms).
 constexpr size_t kScoreChunkBytes = size_t(512) << 20;
 
+// Inside dsa_forward the top-k and attention launches of decode-sized
+// batches (fewer query rows than SMs, rows of at most 64 K positions) are
+// programmatic dependents of the launch before them: their CTAs become
+// resident while that kernel drains, and wait for it before reading its
+// results (64 x 32,768 decode step 154.6 -> 151.2 us).  Many-row prefills
+// and cluster-split long rows ran slightly slower chained (7.72 -> 7.74 ms,
+// 120.8 -> 121.7 us), so they launch plainly.
+bool chain_launches(const dsa_batch* b) {
+    return (int64_t)b->batch * b->max_q < kNumSMs && b->max_ctx <= 65536;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -105,16 +116,18 @@ dsa_status forward_impl(const dsa_batch* batch, ScoreFn score, const uint16_t* q
     const int64_t sc_ld = scores_out ? ld : L.ld_s;
     // indices by packed row (idx_out, or the workspace buffer of every row)
     int32_t* ix = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + L.off_idx);
+    const bool chain = chain_launches(batch);
     // scores and top-k chunk by chunk, then one attention launch over every
     // row (no per-chunk wave tails)
     for (int32_t i0 = 0; i0 < batch->max_q; i0 += L.chunk_rows) {
         const RowRange rr{i0, std::min(i0 + L.chunk_rows, batch->max_q)};
         cudaError_t e = score(rr, sc, sc_ld, scores_out == nullptr);
-        if (e == cudaSuccess) e = launch_topk(bd, rr, sc, sc_ld, scores_out == nullptr, k, ix, false, status, s);
+        if (e == cudaSuccess)
+            e = launch_topk(bd, rr, sc, sc_ld, scores_out == nullptr, k, ix, false, status, s, chain);
         if (e != cudaSuccess) return cuda_status(e);
     }
     return cuda_status(launch_sparse_mla(bd, RowRange{0, batch->max_q}, q, kv, ix, false, k, sm_scale, out, lse,
-                                         base + L.off_attn, L.attn_bytes, status, s));
+                                         base + L.off_attn, L.attn_bytes, status, s, chain));
 }
 
 // Host checks shared by the forward calls (everything but the indexer inputs).

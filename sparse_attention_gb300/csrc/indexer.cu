@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ, kFp8>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+    pdl_launch_dependents();     // a dependent top-k may start launching
     const int b = blockIdx.z;
     SeqInfo sq;
     if (!load_seq(bd, b, status, sq)) return;

@@ -92,9 +92,12 @@ cudaError_t launch_indexer_fp8(const BatchDev& bd, RowRange rr, const uint8_t* q
                                int32_t* status, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(int64_t rows, const uint16_t* in, uint8_t* codes, float* scale, cudaStream_t stream);
 
+// after_previous: launched as a programmatic dependent of the previous
+// kernel in the stream (its CTAs may become resident while that kernel
+// finishes, and wait for it before reading anything).
 cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, int64_t ld,
                         bool scores_local, int k, int32_t* idx, bool idx_local, int32_t* status,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool after_previous = false);
 
 // Bytes of scratch the attention launch needs for `rows` query rows.
 size_t sparse_mla_scratch_bytes(const BatchDev& bd, int64_t rows, int k);
@@ -102,7 +105,7 @@ size_t sparse_mla_scratch_bytes(const BatchDev& bd, int64_t rows, int k);
 cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q, const uint16_t* kv,
                               const int32_t* idx, bool idx_local, int k, float sm_scale,
                               uint16_t* out, float* lse, void* scratch, size_t scratch_bytes,
-                              int32_t* status, cudaStream_t stream);
+                              int32_t* status, cudaStream_t stream, bool after_previous = false);
 
 cudaError_t launch_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const uint16_t* q_pe,
                                 const uint16_t* w_kvb, uint16_t* q_out, int32_t* status, cudaStream_t stream);

@@ -87,6 +87,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel in
+// the stream begin launching once every CTA of this grid has issued it (or
+// exited); wait blocks until the previous grid in the stream has completed
+// and its memory is visible.  Both are no-ops for kernels launched without
+// the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Starts a prefetch into L2 of `bytes` bytes (a multiple of 16) at the
 // 16-byte aligned global address p; nothing is written to shared memory.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {

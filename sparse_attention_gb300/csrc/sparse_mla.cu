@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+    pdl_wait();                  // the indices of the previous launch are complete
     const int b = blockIdx.y;
     SeqInfo sq;
     if (!load_seq(bd, b, status, sq)) return;
@@ -720,7 +721,7 @@ size_t sparse_mla_scratch_bytes(const BatchDev& bd, int64_t rows_per_seq, int k)
 cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q, const uint16_t* kv,
                               const int32_t* idx, bool idx_local, int k, float sm_scale, uint16_t* out,
                               float* lse, void* scratch, size_t scratch_bytes, int32_t* status,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool after_previous) {
     const int32_t rows_per_seq = min(rr.i1, bd.max_q) - rr.i0;
     if (rows_per_seq <= 0) return cudaSuccess;
     const int64_t rows = (int64_t)rows_per_seq * bd.B;
@@ -751,13 +752,15 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cluster_merge ? (unsigned)splits : 1u;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = after_previous ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, bd, rr, tm_q, kv, idx, idx_local ? 1 : 0, k, rows_per_seq,
                            splits, per_split, l2_prefetch, cluster_merge ? 1 : 0, sm_scale, out, lse, part_o,
                            part_lse, status);

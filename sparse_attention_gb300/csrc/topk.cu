@@ -36,6 +36,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -291,6 +292,8 @@ __global__ void __launch_bounds__(NT, NT <= 512 ? 2 : 1)
 
     // every test below depends only on the row, so all CTAs of a cluster
     // take the same branch and reach the same cluster barriers
+    pdl_launch_dependents();     // a dependent attention may start launching
+    pdl_wait();                  // the scores of the previous launch are complete
     const int b = blockIdx.y;
     SeqInfo sq;
     if (!load_seq(bd, b, status, sq)) return;
@@ -593,7 +596,7 @@ __global__ void __launch_bounds__(NT, NT <= 512 ? 2 : 1)
 template <int NT>
 cudaError_t launch_nt(const BatchDev& bd, RowRange rr, const float* scores, int64_t ld, bool scores_local, int k,
                       int32_t* idx, bool idx_local, int csize, int32_t rows_per_seq, int32_t* status,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool after_previous) {
     const size_t smem = sizeof(TopkSmem<NT>);
     cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -602,13 +605,15 @@ cudaError_t launch_nt(const BatchDev& bd, RowRange rr, const float* scores, int6
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = after_previous ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, topk_kernel<NT>, bd, rr, scores, ld, scores_local ? 1 : 0, k, idx,
                            idx_local ? 1 : 0, csize, status);
     if (e == cudaSuccess) count_launches(1);
@@ -618,7 +623,8 @@ cudaError_t launch_nt(const BatchDev& bd, RowRange rr, const float* scores, int6
 }  // namespace
 
 cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, int64_t ld, bool scores_local,
-                        int k, int32_t* idx, bool idx_local, int32_t* status, cudaStream_t stream) {
+                        int k, int32_t* idx, bool idx_local, int32_t* status, cudaStream_t stream,
+                        bool after_previous) {
     const int32_t rows_per_seq = min(rr.i1, bd.max_q) - rr.i0;
     if (rows_per_seq <= 0) return cudaSuccess;
     // long rows, few of them: split each row over a cluster
@@ -627,9 +633,9 @@ cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, in
     if (bd.max_ctx > kLongRow && rows < 2 * kNumSMs)
         csize = (int)std::min<int64_t>(kMaxCluster, ((int64_t)bd.max_ctx + kKeysPerCta - 1) / kKeysPerCta);
     return rows < kNumSMs ? launch_nt<1024>(bd, rr, scores, ld, scores_local, k, idx, idx_local, csize, rows_per_seq,
-                                            status, stream)
+                                            status, stream, after_previous)
                           : launch_nt<512>(bd, rr, scores, ld, scores_local, k, idx, idx_local, csize, rows_per_seq,
-                                           status, stream);
+                                           status, stream, after_previous);
 }
 
 }  // namespace dsa
