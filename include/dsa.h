@@ -172,10 +172,10 @@ DSA_API dsa_status dsa_sparse_mla_fwd(const dsa_batch* batch, const uint16_t* q,
 
 /* Step 3 for callers that cannot allocate device memory.  The pages have no
  * counterpart to this call; it exists for integration.  Some callers cannot
- * allocate at the point where attention runs: code inside a CUDA stream
- * capture that must not allocate, serving loops that budget every byte of
- * device memory in advance and treat any allocation as a failure, or
- * embedders whose allocator is not reachable from the calling thread.  This
+ * allocate at the point where attention runs: serving loops that budget
+ * every byte of device memory in advance and treat any allocation as a
+ * failure, or embedders whose allocator is not reachable from the calling
+ * thread.  This
  * call computes exactly what dsa_sparse_mla_fwd computes (same kernels, same
  * split of each query's selected list, so the same bits), but it takes no
  * workspace: its split-K partials live in a 32 MiB array of static device
@@ -192,7 +192,10 @@ DSA_API dsa_status dsa_sparse_mla_fwd(const dsa_batch* batch, const uint16_t* q,
  * k = 2048); 8 rows x 16 splits take 16.8 MB; 100 rows x 3 splits (k = 2047)
  * do not fit.
  * The first call on a device looks up the array's device address (once per
- * device); make that first call before any stream capture.  Every call on a
+ * device); make that first call before any stream capture.  The address
+ * stays cached for the process: after cudaDeviceReset this call must not be
+ * used again.  A launch failure returns DSA_ERR_CUDA and is reported by
+ * dsa_last_cuda_error, like every other call.  Every call on a
  * device shares the one array, so calls whose kernels overlap on the GPU
  * (different streams, or different host threads) race and corrupt each
  * other's results: order them on one stream. */

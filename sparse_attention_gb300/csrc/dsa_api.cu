@@ -80,6 +80,14 @@ WsLayout ws_layout(const dsa_batch* b, int k) {
     return L;
 }
 
+dsa_status check_ws(const dsa_batch* b, int k, void* ws, size_t ws_bytes) {
+    if (!ws || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(b, k).total) return DSA_ERR_WORKSPACE;
+    return DSA_OK;
+}
+
+}  // namespace
+
 thread_local cudaError_t t_last_error = cudaSuccess;
 
 dsa_status cuda_status(cudaError_t e) {
@@ -89,13 +97,6 @@ dsa_status cuda_status(cudaError_t e) {
     return DSA_ERR_CUDA;
 }
 
-dsa_status check_ws(const dsa_batch* b, int k, void* ws, size_t ws_bytes) {
-    if (!ws || !aligned16(ws)) return DSA_ERR_WORKSPACE;
-    if (ws_bytes < ws_layout(b, k).total) return DSA_ERR_WORKSPACE;
-    return DSA_OK;
-}
-
-}  // namespace
 }  // namespace dsa
 
 using namespace dsa;

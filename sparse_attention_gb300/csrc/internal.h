@@ -79,6 +79,11 @@ bool make_tmap_u8_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t
 // Adds n to the process-wide count of kernels launched by this library.
 void count_launches(int n);
 
+// DSA_OK for cudaSuccess; otherwise records e as this thread's last CUDA
+// error (dsa_last_cuda_error), clears a non-sticky launch error and returns
+// DSA_ERR_CUDA.
+dsa_status cuda_status(cudaError_t e);
+
 // ------------------------------------------------------------ launchers --
 
 cudaError_t launch_indexer(const BatchDev& bd, RowRange rr, const uint16_t* q_idx, const float* w,

@@ -2,10 +2,9 @@
 // that cannot allocate device memory.
 //
 // Some callers cannot call cudaMalloc at the point where they run attention:
-// code running inside a CUDA stream capture that must not allocate, serving
-// loops that pre-plan every byte of device memory and treat any allocation as
-// a failure, or embedders whose allocator is not reachable from the calling
-// thread.  dsa_sparse_mla_fwd needs a caller-provided workspace for its
+// serving loops that plan every byte of device memory in advance and treat
+// any allocation as a failure, or embedders (a host runtime, a plugin) whose
+// allocator is not reachable from the thread that calls attention.  dsa_sparse_mla_fwd needs a caller-provided workspace for its
 // split-K partials; this entry point instead keeps them in one fixed-size
 // array of static device memory that the library owns.  Every GPU that loads
 // the library holds the array (kNoAllocScratchBytes) until the process exits.
@@ -28,7 +27,10 @@ std::mutex g_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the array on the current device, looked up once per
-// device (the name is only a host-side stand-in for the array).
+// device (the name is only a host-side stand-in for the array).  The cached
+// address belongs to the device's primary context: after cudaDeviceReset
+// the array is loaded again elsewhere, so this call is not usable after a
+// reset in the same process.
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -79,11 +81,7 @@ dsa_status dsa_sparse_mla_fwd_noalloc(const dsa_batch* batch, const uint16_t* q,
     if (e == cudaSuccess)
         e = launch_sparse_mla(bd, RowRange{0, batch->max_q}, q, kv, idx, false, k, sm_scale, out, lse, scratch,
                               kNoAllocScratchBytes, device_status, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return DSA_ERR_CUDA;
-    }
-    return DSA_OK;
+    return cuda_status(e);
 }
 
 }  // extern "C"

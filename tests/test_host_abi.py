@@ -130,3 +130,25 @@ def test_product_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "liboracle" not in text and "oracle.c" not in text, f
+
+
+def test_noalloc_host_checks_and_error_record(lib):
+    """The allocation-free attention call rejects bad arguments on the host,
+    refuses partials beyond its static array before any CUDA call, and a
+    failing CUDA call is reported by dsa_last_cuda_error like every other
+    entry point's."""
+    import torch
+    b = _batch()
+    p = 0x7f0000100000
+    B = ctypes.byref(b)
+    f = lib.dsa_sparse_mla_fwd_noalloc
+    assert f(B, p, p, p, 0, ctypes.c_float(0.0625), p, None, None, None) == 1          # k < 1
+    assert f(B, p + 8, p, p, 8, ctypes.c_float(0.0625), p, None, None, None) == 1      # misaligned q
+    assert f(B, p, p, p, 8, ctypes.c_float(0.0), p, None, None, None) == 1             # bad scale
+    big = _batch(total_q=100, max_q=100, max_ctx=4096, stride=4096)
+    assert f(ctypes.byref(big), p, p, p, 2047, ctypes.c_float(0.0625), p, None, None, None) == 3
+    if torch.cuda.is_available():
+        pytest.skip("the error-record check needs a host without a CUDA device")
+    # no device here: the address lookup fails before anything is launched
+    assert f(B, p, p, p, 8, ctypes.c_float(0.0625), p, None, None, None) == 4          # DSA_ERR_CUDA
+    assert lib.dsa_last_cuda_error() != b"no error"

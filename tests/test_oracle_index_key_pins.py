@@ -64,6 +64,33 @@ def test_index_key_matches_numpy(params):
     assert np.allclose(w, xf @ _wf(params.ww).T / np.sqrt(32.0), rtol=1e-12, atol=1e-14)
 
 
+def test_head_weights_one_hot_rows(params):
+    """weights_proj rows that are one-hot, row h = a_h at column c_h, give
+    w[t, h] = a_h * x[t, c_h] / sqrt(32) exactly ("GLM-5.1 架构深度拆解" §3.6
+    Step 4: the head weight is weights_proj(x) times H_idx^-1/2 with
+    H_idx = 32).  The columns differ per head and the factors per head, so a
+    transposed weight, a reading of x by head index, or any other factor
+    (1/32, sqrt(32), 1/sqrt(128)) fails."""
+    T = 3
+    x = W.make_hidden_np(T, 26)
+    cols = (np.arange(32) * 193 + 7) % 6144
+    a = np.array([(-1.0) ** h * 2.0 ** (h % 5 - 2) for h in range(32)], np.float32)
+    ww = np.zeros((32, 6144), np.uint16)
+    ww[np.arange(32), cols] = W.bf16_bits_from_f32(a)
+    _, w = oracle.index_key(x, params.wk, params.gamma, params.beta, params.eps,
+                            np.ones((T, 64)), np.zeros((T, 64)), ww)
+    xf = _wf(x)
+    for h in range(32):
+        assert np.array_equal(w[:, h], a[h] * xf[:, cols[h]] / np.sqrt(32.0))
+    # a one-hot token x = e_c reads column c of weights_proj: w[h] = ww[h, c] / sqrt(32)
+    c = 4099
+    xe = np.zeros((1, 6144), np.uint16)
+    xe[0, c] = W.bf16_bits_from_f32(np.array([1.0], np.float32))[0]
+    _, w1 = oracle.index_key(xe, params.wk, params.gamma, params.beta, params.eps,
+                             np.ones((1, 64)), np.zeros((1, 64)), params.ww)
+    assert np.array_equal(w1[0], _wf(params.ww)[:, c] / np.sqrt(32.0))
+
+
 def test_wrapper_refuses_wrong_sizes(params):
     x = W.make_hidden_np(2, 25)
     cos, sin = W.rotary_rows([0, 1])

@@ -53,6 +53,57 @@ def test_output_one_hot_and_numpy(weights):
     assert np.allclose(y, o_mid.reshape(T, -1) @ wo.T, rtol=1e-10, atol=1e-12)
 
 
+def _one_hot_uv(h0, e0, d0):
+    """kv_b_proj whose only non-zero entry is W_UV[h0][e0, d0] = 1 (head h0
+    holds rows 448 h0 .. 448 h0 + 447; its last 256 rows are W_UV[h0])."""
+    w = np.zeros((64 * 448, 512), np.uint16)
+    w[448 * h0 + 192 + e0, d0] = W.bf16_bits_from_f32(np.array([1.0], np.float32))[0]
+    return w
+
+
+def test_o_proj_reads_head_major_columns(weights):
+    """o_proj's input is the attention output reshaped head-major to
+    [T, 64 x 256] ("GLM-5.1 架构深度拆解" §4.5 Step 8), so head h's value
+    dimension e is column 256 h + e of W_o.  With o_mid one-hot at (h0, e0)
+    the output is that column exactly; a dimension-major layout would read
+    column 64 e0 + h0 instead."""
+    h0, e0, d0 = 5, 17, 300
+    w_kvb = _one_hot_uv(h0, e0, d0)
+    o_lat = np.zeros((2, 64, 512))
+    o_lat[0, h0, d0] = 1.0
+    o_lat[1, h0, d0] = -3.0
+    o_mid, y = oracle.mla_output(o_lat, w_kvb, weights.w_o)
+    expect_mid = np.zeros((64, 256))
+    expect_mid[h0, e0] = 1.0
+    assert np.array_equal(o_mid[0], expect_mid)
+    wo = _wf(weights.w_o)
+    assert np.array_equal(y[0], wo[:, 256 * h0 + e0])
+    assert np.array_equal(y[1], -3.0 * wo[:, 256 * h0 + e0])
+    assert not np.array_equal(wo[:, 256 * h0 + e0], wo[:, 64 * e0 + h0])
+
+
+def test_expanded_o_proj_reads_head_major_columns(weights):
+    """The same closed form through the pages' expanded path: every query
+    attends to one cached row s0 only, so o_mid[h0, e0] = c[s0][d0] and
+    y = c[s0][d0] * W_o[:, 256 h0 + e0]."""
+    h0, e0, d0 = 9, 200, 4
+    w_kvb = _one_hot_uv(h0, e0, d0)
+    bt, _ = _tiny_batch()
+    idx = np.full((bt.total_q, 8), -1, np.int32)
+    idx[:, 0] = 1
+    qn, qp = W.make_mla_queries_np(bt.total_q, 95)
+    o_mid, y = oracle.mla_expanded(bt, qn, qp, w_kvb, weights.w_o, idx)
+    kv = _wf(bt.kv).reshape(-1, 576)
+    wo = _wf(weights.w_o)
+    for r, (b, t) in enumerate(bt.positions()):
+        c = kv[b * bt.stride + 1, d0]
+        assert c != 0.0
+        expect_mid = np.zeros((64, 256))
+        expect_mid[h0, e0] = c
+        assert np.array_equal(o_mid[r], expect_mid)
+        assert np.array_equal(y[r], c * wo[:, 256 * h0 + e0])
+
+
 def _tiny_batch():
     # two sequences, ragged, selections with -1 holes; cached rows N(0,1)
     bt = W.make_batch_np([40, 23], [3, 2], k=8, seed=91)

@@ -3,9 +3,10 @@ called through the C ABI, against the workspace entry point on the same
 inputs, two calls in a row.
 
 It serves callers that cannot allocate device memory where attention runs
-(inside a stream capture, or under a fixed memory plan): its split-K
-partials live in the library's static device scratch instead of a
-caller-provided workspace.  This file is collected last on purpose.
+(a serving loop under a fixed memory plan, or an embedder without access to
+the allocator): its split-K partials live in the library's static device
+scratch instead of a caller-provided workspace.  This file is collected last
+on purpose.
 """
 
 import ctypes
