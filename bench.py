@@ -38,6 +38,9 @@ import workloads as W  # noqa: E402
 
 DEFAULT_WORKLOAD = "decode_B64_ctx32768"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}     # GB300 data-sheet figures, for context
+# workloads timed beside the default decode line (details.other_workloads)
+SIDE_WORKLOADS = ("prefill_T16384", "long_decode_B8_ctx202752")
 
 # algorithmic work per unit
 IDX_FLOP_PER_PAIR = 2 * 32 * 128            # 8192
@@ -70,6 +73,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--kernel-reps", type=int, default=20)
+    p.add_argument("--no-side", action="store_true", help="skip the prefill / long-decode sets of the default line")
     return p.parse_args()
 
 
@@ -350,6 +354,75 @@ class Case:
         return work
 
 
+def step_roofline(case: "Case", ms_step: float, peaks):
+    """The whole step against its roofline: algorithmic bytes (HBM-bound
+    decode) or flops (tensor-bound prefill) of one step over the step's
+    time, as a fraction of the measured peak and of the nominal one."""
+    wk, wl = case.work(), case.wl
+    if wl.base in ("decode", "indexshare"):
+        b = wk["idx_bytes"] + wk["att_bytes"] + wk["mla_bytes"]
+        ach = b / (ms_step * 1e-3) / 1e9
+        return {"bound": "hbm", "algorithmic": b, "achieved": ach, "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "frac_nominal": ach / NOMINAL_PEAKS["hbm_gbs"]}
+    f = wk["idx_flop"] + wk["att_flop"] + wk["mla_flop"]
+    ach = f / (ms_step * 1e-3) / 1e12
+    return {"bound": "tensor", "algorithmic": f, "achieved": ach, "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"], "frac_nominal": ach / NOMINAL_PEAKS["bf16_tflops"]}
+
+
+def timed_steps(case: "Case", K: int, stream):
+    """K steps between CUDA events on the launching stream (one event after
+    every step): total milliseconds and the per-step times."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    evs[0].record(stream)
+    for i in range(K):
+        case.step(i)
+        evs[i + 1].record(stream)
+    return evs
+
+
+def per_step_ms(evs):
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(len(evs) - 1)]
+
+
+def side_workload(name: str, dev, peaks, reps: int):
+    """One more workload timed in the same run (warm-up 3, then 10 steps for
+    a prefill or 200 for a decode step), with its kernel times and its
+    whole-step roofline fraction."""
+    import torch
+    wl = W.WORKLOADS[name]
+    case = Case(wl, wl.seed, dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    for i in range(3):
+        case.step(i)
+    torch.cuda.synchronize()
+    K = 200 if wl.base == "decode" else 10
+    t0 = time.time()
+    evs = timed_steps(case, K, stream)
+    torch.cuda.synchronize()
+    clocks.timed(t0, time.time())
+    ms = evs[0].elapsed_time(evs[-1])
+    steps = per_step_ms(evs)
+    t0 = time.time()
+    for i in range(max(1, int(0.3 / (ms / K / 1e3)))):
+        case.step(i)
+    torch.cuda.synchronize()
+    clocks.hold(t0, time.time())
+    times = case.kernel_times_us(reps)
+    clk = clocks.stop()
+    status = case.dsa.read_device_status(case.ws[0])
+    res = {"metric": case.metric, "value": case.units_per_step * K / (ms / 1e3), "unit": case.unit, "steps": K,
+           "warmup": 3, "ms_per_step": ms / K, "ms_per_step_median": statistics.median(steps),
+           "step_roofline": step_roofline(case, ms / K, peaks),
+           "kernel_us": {k: round(v, 2) for k, v in times.items()}, "device_status": status, "clocks": clk}
+    del case
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
@@ -364,6 +437,7 @@ class ClockSampler:
         self.gpu_index = gpu_index
         self.proc = None
         self.window = None
+        self.hold_window = None
 
     def start(self):
         try:
@@ -375,6 +449,9 @@ class ClockSampler:
 
     def timed(self, t0: float, t1: float):
         self.window = (t0, t1)
+
+    def hold(self, t0: float, t1: float):
+        self.hold_window = (t0, t1)
 
     def stop(self):
         if not self.proc:
@@ -389,12 +466,20 @@ class ClockSampler:
                 continue
             try:
                 ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                samples.append((ts, float(r[1]), float(r[2]), r[5:9]))
+                samples.append((ts, float(r[1]), float(r[2]), tuple(r[5:9])))
             except ValueError:
                 continue
-        inside = [x for x in samples if self.window and self.window[0] - 0.05 <= x[0] <= self.window[1] + 0.05]
+        def within(w):
+            return [x for x in samples if w and w[0] - 0.05 <= x[0] <= w[1] + 0.05]
+
+        inside = within(self.window)
         scope = "timed region"
-        if len(inside) < 2:      # a short timed region: use the busy period around it
+        if len(inside) < 2:
+            # a short timed region: add the ~0.5 s repeat of the same steps
+            # that follows it
+            inside = sorted(set(inside) | set(within(self.hold_window)))
+            scope = "timed region and a 0.5 s repeat of the same steps right after it"
+        if len(inside) < 2:
             inside, scope = samples, "warm-up, timed region and per-kernel timing"
         sm = [x[1] for x in inside]
         reasons = sorted({n for x in inside for n, v in zip(self.REASONS, x[3]) if v.lower() == "active"})
@@ -546,7 +631,8 @@ def run_reference(args):
     value = frac / secs
     metric, unit = metric_for(wl)
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
-            "steps": K, "warmup": Wu, "ms_per_step": 1e3 / value if unit == "steps/s" else 1e3 * secs,
+            "steps": K, "warmup": Wu, "ms_per_step": 1e3 * secs,
+            "ms_per_full_step_extrapolated": 1e3 / value if unit == "steps/s" else 1e3 * wl.ctx / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": base_config(wl, 1),
             "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
@@ -634,19 +720,24 @@ def run_dsa(args):
         case.step(i)
     barrier()
     n0 = dsa.kernel_launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     t_start = time.time()
-    e0.record(stream)
-    for i in range(K):
-        case.step(i)
-    e1.record(stream)
+    evs = timed_steps(case, K, stream)
     barrier()
     clocks.timed(t_start, time.time())
     launches = dsa.kernel_launch_count() - n0
-    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    ms = max_over_ranks(evs[0].elapsed_time(evs[-1]), dev)
+    step_ms = per_step_ms(evs)
     status = dsa.read_device_status(case.ws[0])
     value = whole_job_value(case.units_per_step, K, world, ms)
+    # a short timed region holds few clock samples: repeat the same steps
+    # for about half a second under the sampler (not timed)
+    t_hold = time.time()
+    n_hold = max(1, int(0.5 / max(ms / K / 1e3, 1e-6)))
+    for i in range(n_hold):
+        case.step(i)
+    barrier()
+    clocks.hold(t_hold, time.time())
 
     # end to end through the public API with host buffers
     e2e = None
@@ -669,16 +760,19 @@ def run_dsa(args):
         achieved = kw["bytes"] / (times[dom] * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
+    sr = step_roofline(case, ms / K, peaks)
     roof.update({"kernel": dom, "peak_source": f"{peak_src} ({'burst' if roof['bound'] == 'tensor' else 'copy'})",
                  "traffic": traffic_from_profiles(dom, wl.name),
                  "kernel_us": {k: round(v, 2) for k, v in times.items()},
-                 "algorithmic_per_launch": kw})
+                 "algorithmic_per_launch": kw,
+                 "step_frac": sr["frac"], "step_frac_nominal": sr["frac_nominal"], "step": sr})
 
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1 and wl.base != "indexshare":
         cpu = cpu_baseline(case, case.unit)
+    case_metric, case_unit = case.metric, case.unit
     wk = case.work()
     cfg = base_config(wl, world)
     details = {"algorithmic_per_step": {"indexer_tflop": wk["idx_flop"] / 1e12,
@@ -691,7 +785,14 @@ def run_dsa(args):
         details["mla_device_status"] = dsa.read_device_status(case.mla_ws)
     if wl.base in ("decode", "indexshare"):
         details["tokens_per_s"] = value * wl.B
-    line = {"metric": case.metric, "value": value, "unit": case.unit, "n_gpus": world, "steps": K, "warmup": Wu,
+    details["ms_per_step_median"] = statistics.median(step_ms)
+    if wl.name == DEFAULT_WORKLOAD and world == 1 and not args.no_side:
+        # the metric's other half (prefill tokens/s) and the long-context
+        # decode, timed in the same run
+        del case
+        torch.cuda.empty_cache()
+        details["other_workloads"] = {n: side_workload(n, dev, peaks, args.kernel_reps) for n in SIDE_WORKLOADS}
+    line = {"metric": case_metric, "value": value, "unit": case_unit, "n_gpus": world, "steps": K, "warmup": Wu,
             "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": cfg, "roofline": roof, "cpu_baseline": cpu,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "details": details}

@@ -30,7 +30,7 @@ constexpr size_t kScoreChunkBytes = size_t(512) << 20;
 // and cluster-split long rows ran slightly slower chained (7.72 -> 7.74 ms,
 // 120.8 -> 121.7 us), so they launch plainly.
 bool chain_launches(const dsa_batch* b) {
-    return (int64_t)b->batch * b->max_q < kNumSMs && b->max_ctx <= 65536;
+    return (int64_t)b->batch * b->max_q < num_sms() && b->max_ctx <= 65536;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -89,6 +89,25 @@ dsa_status check_ws(const dsa_batch* b, int k, void* ws, size_t ws_bytes) {
 }  // namespace
 
 thread_local cudaError_t t_last_error = cudaSuccess;
+
+int num_sms() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return kDefaultSMs;
+    }
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return kDefaultSMs;
+    }
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 dsa_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return DSA_OK;

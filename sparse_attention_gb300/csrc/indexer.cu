@@ -300,7 +300,8 @@ cudaError_t launch_nq(const BatchDev& bd, RowRange rr, const void* q_idx, const 
         // decode-like: spread every sequence's key stream over enough CTAs
         // for ~4 CTAs per SM in total
         const int64_t total = (int64_t)tiles * groups * bd.B;
-        tps = (int)std::max<int64_t>(4, (total + 4 * kNumSMs - 1) / (4 * kNumSMs));
+        const int64_t nsm = num_sms();
+        tps = (int)std::max<int64_t>(4, (total + 4 * nsm - 1) / (4 * nsm));
     }
     const int32_t splits = (tiles + tps - 1) / tps;
     CUtensorMap tm_k, tm_q;

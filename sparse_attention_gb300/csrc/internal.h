@@ -16,7 +16,7 @@ constexpr int kH = DSA_HEADS;            // 64 attention heads
 constexpr int kDQK = DSA_QK_DIM;         // 576 = 512 latent + 64 rope
 constexpr int kDV = DSA_V_DIM;           // 512
 constexpr int kMaxTopk = DSA_MAX_TOPK;   // 2048
-constexpr int kNumSMs = 152;             // GB300
+constexpr int kDefaultSMs = 152;         // GB300: used when no device can be queried
 
 // Upper bound on any single in-kernel wait (a phase of an mbarrier).  A wait
 // that exceeds it latches DSA_ERR_TIMEOUT and the kernel winds down.
@@ -75,6 +75,10 @@ bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64
 // The same for a 2-D tensor of bytes (row stride inner bytes).
 bool make_tmap_u8_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                      uint32_t box_rows);
+
+// Streaming multiprocessors of the current device (cudaDevAttrMultiProcessorCount,
+// read once per device); kDefaultSMs when no device can be queried.
+int num_sms();
 
 // Adds n to the process-wide count of kernels launched by this library.
 void count_launches(int n);

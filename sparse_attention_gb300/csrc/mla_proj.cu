@@ -311,8 +311,8 @@ __global__ void copy_rope_kernel(int64_t rows, const uint4* __restrict__ q_pe, u
 int choose_k_splits(int32_t M, int32_t N, int32_t K, int32_t batches) {
     const int64_t tiles = (int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN) * batches;
     const int32_t nk = K / kBK;
-    if (tiles == 0 || tiles * 2 > kNumSMs) return 1;
-    return (int)std::max<int64_t>(1, std::min<int64_t>(nk / 8, kNumSMs / tiles));
+    if (tiles == 0 || tiles * 2 > num_sms()) return 1;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(nk / 8, num_sms() / tiles));
 }
 
 template <bool kBMn>
@@ -326,14 +326,14 @@ cudaError_t launch_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b, GemmAr
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<kBMn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int grid = (int)std::min<int64_t>(tiles, kNumSMs);
+    const int grid = (int)std::min<int64_t>(tiles, num_sms());
     gemm_bf16_kernel<kBMn><<<grid, kThreads, kSmemBytes, stream>>>(tm_a, tm_b, g, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1);
     if (g.splits == 1 || g.out_fp32) return cudaSuccess;
     const int64_t n8 = (int64_t)g.M * g.ldc / 8;
-    const int blocks = (int)std::min<int64_t>((n8 + 255) / 256, 8 * kNumSMs);
+    const int blocks = (int)std::min<int64_t>((n8 + 255) / 256, 8 * num_sms());
     reduce_kernel<<<blocks, 256, 0, stream>>>(g.M, g.ldc, g.splits, g.part, g.C);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
@@ -392,7 +392,7 @@ cudaError_t launch_mla_absorb_q(int32_t total_q, const uint16_t* q_nope, const u
     cudaError_t e = launch_gemm<true>(tm_a, tm_b, g, status, stream);
     if (e != cudaSuccess) return e;
     const int64_t pieces = (int64_t)total_q * kH * 8;
-    const int blocks = (int)std::min<int64_t>((pieces + 255) / 256, 16 * kNumSMs);
+    const int blocks = (int)std::min<int64_t>((pieces + 255) / 256, 16 * num_sms());
     copy_rope_kernel<<<blocks, 256, 0, stream>>>((int64_t)total_q * kH, reinterpret_cast<const uint4*>(q_pe), q_out);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);

@@ -685,15 +685,16 @@ __global__ void __launch_bounds__(256)
 }
 
 // CTAs per query row.  One CTA fills an SM's shared memory, so the grid
-// runs in waves of kNumSMs CTAs; pick the split count that minimises
+// runs in waves of num_sms() CTAs; pick the split count that minimises
 // waves x (blocks per CTA + one block's worth of per-CTA overhead).
 int choose_splits(int64_t rows, int k) {
     if (rows <= 0) return 1;
     const int nblk = std::max(1, (k + kBlk - 1) / kBlk);
+    const int64_t nsm = num_sms();
     int best = 1;
     int64_t best_cost = -1;
     for (int sp = 1; sp <= std::min(16, nblk); ++sp) {
-        const int64_t waves = (rows * sp + kNumSMs - 1) / kNumSMs;
+        const int64_t waves = (rows * sp + nsm - 1) / nsm;
         const int64_t cost = waves * ((nblk + sp - 1) / sp + 1);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;

@@ -630,9 +630,9 @@ cudaError_t launch_topk(const BatchDev& bd, RowRange rr, const float* scores, in
     // long rows, few of them: split each row over a cluster
     const int64_t rows = (int64_t)rows_per_seq * bd.B;
     int csize = 1;
-    if (bd.max_ctx > kLongRow && rows < 2 * kNumSMs)
+    if (bd.max_ctx > kLongRow && rows < 2 * num_sms())
         csize = (int)std::min<int64_t>(kMaxCluster, ((int64_t)bd.max_ctx + kKeysPerCta - 1) / kKeysPerCta);
-    return rows < kNumSMs ? launch_nt<1024>(bd, rr, scores, ld, scores_local, k, idx, idx_local, csize, rows_per_seq,
+    return rows < num_sms() ? launch_nt<1024>(bd, rr, scores, ld, scores_local, k, idx, idx_local, csize, rows_per_seq,
                                             status, stream, after_previous)
                           : launch_nt<512>(bd, rr, scores, ld, scores_local, k, idx, idx_local, csize, rows_per_seq,
                                            status, stream, after_previous);
