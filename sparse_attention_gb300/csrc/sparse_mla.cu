@@ -32,19 +32,20 @@
 //               taken (warp max by redux.sync, then across lane quarters)
 //               and O^T rescaled in TMEM.  p = 2^(s*c - m) in fp32, written
 //               as bf16 P^T over the RoPE chunk (free once S^T is done);
-//               final normalisation into the (then free) row tile, copied
-//               out with 16-byte stores: the row's [64 heads, 512] block is
-//               contiguous in the output and in the split partials.
+//               final normalisation straight from TMEM into the output (or
+//               a split's fp32 partial), one column per thread
 // A single 144 KiB row tile fits next to Q (72 KiB); it is refilled chunk
 // by chunk as soon as the MMAs that read each chunk have completed.
 // Split-K partials (for few query rows): with 2 or 4 splits the CTAs of a
-// row form a cluster and merge through distributed shared memory (each CTA
-// combines every split's staged rows for a quarter or half of the heads);
-// more splits write fp32 partials that merge_kernel combines.
+// row form a cluster; each rank merges a share of the heads from its own
+// TMEM and the other ranks' weighted contributions, which arrive by one
+// bulk copy per peer (no scratch memory).  More splits write fp32 partials
+// that merge_kernel combines.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <cmath>
 
 #include "internal.h"
@@ -60,11 +61,25 @@ constexpr int kChunks = kDQK / 64;           // 9 column chunks of 64
 constexpr int kVChunks = kDV / 64;           // the first 8 hold V
 constexpr int kKVChunkBytes = kBlk * 128;    // 16 KiB
 constexpr int kQChunkBytes = kH * 128;       // 8 KiB
-constexpr int kProducerWarps = 2;
+#ifndef DSA_ATTN_PRODUCER_WARPS
+#define DSA_ATTN_PRODUCER_WARPS 2
+#endif
+#ifndef DSA_ATTN_SOFTMAX_WARPS
+#define DSA_ATTN_SOFTMAX_WARPS 8
+#endif
+constexpr int kProducerWarps = DSA_ATTN_PRODUCER_WARPS;
+constexpr int kProducerRows = kBlk / (4 * kProducerWarps);   // rows of a block per producer lane
 constexpr int kMmaWarp = kProducerWarps;                  // warp 2
 constexpr int kSoftmaxWarp0 = kMmaWarp + 1;               // warps 3..10
-constexpr int kSoftmaxThreads = 256;
+constexpr int kSoftmaxWarps = DSA_ATTN_SOFTMAX_WARPS;     // two (or four) per TMEM lane quarter
+constexpr int kHPT = kH * 4 / kSoftmaxWarps;              // heads per softmax thread: 32
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kThreads = 32 * kSoftmaxWarp0 + kSoftmaxThreads;   // 352
+static_assert(kHPT == 16 || kHPT == 32, "the softmax loads S^T and O^T 16 or 32 columns at a time");
+
+// kHPT TMEM columns of this thread's lane from taddr
+__device__ __forceinline__ void tmem_ld_hpt(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld_32x32b_x32(taddr, r); }
+__device__ __forceinline__ void tmem_ld_hpt(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld_32x32b_x16(taddr, r); }
 constexpr int64_t kL2PrefetchBytes = int64_t(128) << 20;  // cache bytes above which rows are prefetched
 constexpr int kPrefetchAhead = 1;                         // blocks prefetched ahead of the gather
 constexpr int kMaxClusterMerge = 4;                       // most splits merged inside a cluster
@@ -91,7 +106,8 @@ constexpr int kBarP = kBarS + 1;                              // P^T written (on
 constexpr int kBarO = kBarP + 1;                              // PV of a block done (chunk 8 free)
 constexpr int kBarIdx = kBarO + 1;                            // [2]: indices of a block published
 constexpr int kBarDrain = kBarIdx + 2;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarRecv = kBarDrain + 1;                       // cluster merge: the peers' contributions landed
+constexpr int kNumBars = kBarRecv + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;
@@ -179,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kBarP), kSoftmaxThreads / 32);
         mbar_init(bar(kBarIdx), 1);
         mbar_init(bar(kBarIdx + 1), 1);
+        // a row merged in a cluster receives, from every other split, its
+        // contribution to the heads this CTA merges (bf16, kH / splits heads)
+        if (cluster_merge)
+            mbar_arrive_expect_tx(bar(kBarRecv), (uint32_t)((splits - 1) * (kH / splits) * kDV * 2));
         for (int c = 0; c < kChunks; ++c) mbar_init(bar(kBarKV + c), 32 * kProducerWarps);
         misc[1] = 0;
         misc[2] = 0;
@@ -207,12 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kProducerWarps) {
         // ----------------------------------------------------------- producers
-        // producer lane gl = (rq, piece): rows 8n + rq of the block, 16-byte
+        // producer lane gl = (rq, piece): rows 16n + rq of the block, 16-byte
         // piece `piece` of each 128-byte row chunk; 8 lanes cover one row
-        // chunk (coalesced) and row r % 8 == rq fixes the swizzle
+        // chunk (coalesced) and row r % 8 == rq % 8 fixes the swizzle
         const int gl = (int)threadIdx.x;
         const int rq = gl >> 3, piece = gl & 7;
-        const uint32_t dpat = (uint32_t)(rq * 128 + ((piece ^ rq) << 4));
+        const uint32_t dpat = (uint32_t)(rq * 128 + ((piece ^ (rq & 7)) << 4));
         bool ok = true;
         for (int jb = 0; jb < nblk; ++jb) {
             const uint32_t ph = (uint32_t)jb & 1u;
@@ -265,10 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            uint32_t soff[kBlk / 8];   // byte offset of each of this lane's rows (+ piece)
+            uint32_t soff[kProducerRows];   // byte offset of each of this lane's rows (+ piece)
 #pragma unroll
-            for (int n = 0; n < kBlk / 8; ++n) {
-                const int32_t sv = ib[8 * n + rq];
+            for (int n = 0; n < kProducerRows; ++n) {
+                const int32_t sv = ib[4 * kProducerWarps * n + rq];
                 soff[n] = (uint32_t)(sv >= 0 ? sv : 0) * (uint32_t)(kDQK * 2) + (uint32_t)(piece * 16);
             }
             for (int c = 0; c < kChunks; ++c) {
@@ -283,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t* src = kv_seq + c * 128;
                 const uint32_t dst = sKV + c * kKVChunkBytes + dpat;
 #pragma unroll
-                for (int n = 0; n < kBlk / 8; ++n) cp_async_16(dst + 1024u * n, src + soff[n]);
+                for (int n = 0; n < kProducerRows; ++n)
+                    cp_async_16(dst + (uint32_t)(512 * kProducerWarps) * n, src + soff[n]);
                 cp_async_arrive(bar(kBarKV + c));
             }
             // both producer warps agree before either starts the next block
@@ -364,15 +385,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------------- softmax
-        // warp w: TMEM lane quarter w % 4 (rows), head half (w - 3) / 4
+        // warp w: TMEM lane quarter w % 4 (rows), head group (w - 5) / 4 of
+        // kHPT heads
         const uint32_t lq = warp & 3u;
-        const int h0 = ((int)(warp - kSoftmaxWarp0) >> 2) * 32;
+        const int h0 = ((int)(warp - kSoftmaxWarp0) >> 2) * kHPT;
         const int r = (int)(lq * 32 + lane);           // row of the block
-        const int st = (int)threadIdx.x - 32 * kSoftmaxWarp0;   // 0..255 among the softmax threads
+        const int st = (int)threadIdx.x - 32 * kSoftmaxWarp0;   // 0..511 among the softmax threads
         const uint32_t lane_base = (lq * 32u) << 16;
-        float lsum[32];
+        float lsum[kHPT];
 #pragma unroll
-        for (int x = 0; x < 32; ++x) lsum[x] = 0.f;
+        for (int x = 0; x < kHPT; ++x) lsum[x] = 0.f;
         bool ok = true;
         for (int jb = 0; jb < nblk; ++jb) {
             const uint32_t ph = (uint32_t)jb & 1u;
@@ -386,20 +408,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const bool valid = s_idx[(jb & 1) * kBlk + r] >= 0;
-            float s[32];
+            float s[kHPT];
             {
-                uint32_t u[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + h0, u);
+                uint32_t u[kHPT];
+                tmem_ld_hpt(tmem + lane_base + kTmemS + h0, u);
                 tmem_ld_wait();
 #pragma unroll
-                for (int x = 0; x < 32; ++x) s[x] = valid ? __uint_as_float(u[x]) : -INFINITY;
+                for (int x = 0; x < kHPT; ++x) s[x] = valid ? __uint_as_float(u[x]) : -INFINITY;
             }
             // the running max moves only when a score exceeds it by 2^8; the
             // vote compares raw scores with (m + 8) / c2 per head (a trigger
             // only: the exact block max below decides whether m moves)
             bool exceed = false;
 #pragma unroll
-            for (int x = 0; x < 32; x += 4) {
+            for (int x = 0; x < kHPT; x += 4) {
                 const float4 tv = *reinterpret_cast<const float4*>(s_thr + h0 + x);
                 exceed |= s[x] > tv.x;
                 exceed |= s[x + 1] > tv.y;
@@ -409,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (named_bar_or(2, kSoftmaxThreads, exceed)) {
                 // exact per-head block max: warp max, then across lane quarters
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
+                for (int x = 0; x < kHPT; ++x) {
                     const float mx = warp_max_f32(s[x]);
                     if (lane == 0) s_wmax[lq * kH + h0 + x] = mx;
                 }
@@ -439,10 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (jb > 0) {
                         tc_fence_after();
 #pragma unroll 1
-                        for (int piece = 0; piece < 8; ++piece) {      // 4 dv blocks x 2 halves
+                        for (int piece = 0; piece < 4 * (kHPT / 16); ++piece) {   // 4 dv blocks x kHPT heads
                             uint32_t u[16];
-                            const int hx = (piece & 1) * 16;
-                            const uint32_t ta = tmem + lane_base + kTmemO + (piece >> 1) * kH + h0 + hx;
+                            const int hx = (piece % (kHPT / 16)) * 16;
+                            const uint32_t ta = tmem + lane_base + kTmemO + (piece / (kHPT / 16)) * kH + h0 + hx;
                             tmem_ld_32x32b_x16(ta, u);
                             tmem_ld_wait();
 #pragma unroll
@@ -453,13 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st_wait();
                     }
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) lsum[x] *= s_alpha[h0 + x];
+                    for (int x = 0; x < kHPT; ++x) lsum[x] *= s_alpha[h0 + x];
                 }
             }
-            // P^T row r, heads h0..h0+31: 4 swizzled 16-byte pieces (MN-major B)
-            uint8_t* prow = smem + kOffKV + kVChunks * kKVChunkBytes + r * 128;
+            // P^T row r, heads h0..h0+15: 2 swizzled 16-byte pieces (MN-major B)
+            uint8_t* p_row = smem + kOffKV + kVChunks * kKVChunkBytes + r * 128;
 #pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
+            for (int e4 = 0; e4 < kHPT / 8; ++e4) {
                 const float4 ma = *reinterpret_cast<const float4*>(s_m + h0 + e4 * 8);
                 const float4 mb = *reinterpret_cast<const float4*>(s_m + h0 + e4 * 8 + 4);
                 const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
@@ -476,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk.z = pack_bf16x2(p[4], p[5]);
                 pk.w = pack_bf16x2(p[6], p[7]);
                 const int c8 = (h0 >> 3) + e4;
-                *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = pk;
+                *reinterpret_cast<uint4*>(p_row + ((c8 ^ (r & 7)) << 4)) = pk;
             }
             // one arrival per warp once all its lanes' P^T writes are fenced
             fence_proxy_async_smem();
@@ -491,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- epilogue
         // l: the per-thread partial sums reduced over the 128 rows
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
+        for (int x = 0; x < kHPT; ++x) {
             float v = lsum[x];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -514,114 +536,166 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         named_bar_sync(1, kSoftmaxThreads);
-        if (w) {
-            // every MMA has completed (PV of the last block), so the row tile
-            // is free: stage the normalised [64 heads, 512] block there
-            // (bf16 output, or fp32 split partial), then copy it out
+        if (w && !cluster_merge) {
+            // every MMA has completed (PV of the last block): each thread
+            // stores its output column d of its heads straight from TMEM
+            // (per head a warp writes 32 consecutive columns: 64 bytes of
+            // bf16 output or 128 bytes of an fp32 split partial)
             tc_fence_after();
-            float inv[32];                                    // 1 / l of this thread's heads
+            float inv[kHPT];                                  // 1 / l of this thread's heads
 #pragma unroll
-            for (int x = 0; x < 32; x += 4) {
+            for (int x = 0; x < kHPT; x += 4) {
                 const float4 v = *reinterpret_cast<const float4*>(s_l + 5 * kH + h0 + x);
                 inv[x] = v.x;
                 inv[x + 1] = v.y;
                 inv[x + 2] = v.z;
                 inv[x + 3] = v.w;
             }
-            uint16_t* stage_b = reinterpret_cast<uint16_t*>(smem + kOffKV);
-            float* stage_f = reinterpret_cast<float*>(smem + kOffKV);
+            uint16_t* ob = out + (grow * kH + h0) * kDV;
+            float* po = splits > 1 ? part_o + (prow * kH + h0) * kDV : nullptr;
             for (int dv = 0; dv < 4; ++dv) {
                 const int d = dv * 128 + r;                   // output column of this thread
-                uint32_t u[32];
+                uint32_t u[kHPT];
                 if (nblk > 0) {
-                    tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + dv * kH + h0, u);
+                    tmem_ld_hpt(tmem + lane_base + kTmemO + dv * kH + h0, u);
                     tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) u[x] = 0u;
+                    for (int x = 0; x < kHPT; ++x) u[x] = 0u;
                 }
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int h = h0 + x;
+                for (int x = 0; x < kHPT; ++x) {
                     const float o = __uint_as_float(u[x]) * inv[x];
                     if (splits == 1) {
-                        const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-                        stage_b[h * kDV + d] = *reinterpret_cast<const uint16_t*>(&ob);
+                        const __nv_bfloat16 b16 = __float2bfloat16_rn(o);
+                        ob[x * kDV + d] = *reinterpret_cast<const uint16_t*>(&b16);
                     } else {
-                        stage_f[h * kDV + d] = o;
+                        po[x * kDV + d] = o;
                     }
                 }
-            }
-            named_bar_sync(1, kSoftmaxThreads);
-            if (cluster_merge) {
-                if (st == 0) misc[2] = 1u;                    // staged: the cluster may read it
-            } else {
-                const uint32_t bytes = splits == 1 ? kH * kDV * 2 : kH * kDV * 4;
-                uint4* dst = splits == 1 ? reinterpret_cast<uint4*>(out + grow * kH * kDV)
-                                         : reinterpret_cast<uint4*>(part_o + prow * kH * kDV);
-                const uint4* src = reinterpret_cast<const uint4*>(smem + kOffKV);
-                for (uint32_t o = (uint32_t)st; o < bytes / 16; o += kSoftmaxThreads) dst[o] = src[o];
             }
         }
     }
 
     if (cluster_merge) {
-        // The row's splits are the CTAs of this cluster, rank = split.  Each
-        // merges heads h = rank (mod splits) from every split's staged rows:
-        // out = sum_s exp(lse_s - m) o_s / sum_s exp(lse_s - m), m = max lse_s
-        // (the arithmetic of merge_kernel, in the same order).
+        // The row's splits are the CTAs of this cluster, rank = split; rank
+        // sp merges the heads h = sp (mod splits):
+        //   out[h] = sum_s f_s[h] o_s[h],  f_s = exp(lse_s - m) / sum_s' exp(lse_s' - m),
+        // o_s the split's normalised output, m = max_s lse_s, summed in split
+        // order.  Distributed shared memory moves ~14 bytes per clock, so
+        // only the lse values and, for each peer, its heads of this split's
+        // weighted contribution f_s o_s in bf16 cross the cluster (one bulk
+        // copy per peer into its then free Q region); a CTA's own term is
+        // taken in fp32 straight from TMEM.
         cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();                                       // every split has staged (or failed)
+        cluster.sync();                      // every split's lse is staged, its Q region free
         if (warp >= kSoftmaxWarp0) {
             const int st = (int)threadIdx.x - 32 * kSoftmaxWarp0;
-            const uint32_t* flag = reinterpret_cast<const uint32_t*>(smem + kOffMisc) + 2;
-            bool all = true;
-            for (int s2 = 0; s2 < splits; ++s2) all = all && *cluster.map_shared_rank(flag, (unsigned)s2) != 0u;
-            if (all) {
-                const float* r_lse[kMaxClusterMerge];
-                const float4* r_o[kMaxClusterMerge];
+            const uint32_t lq = warp & 3u;
+            const int h0 = ((int)(warp - kSoftmaxWarp0) >> 2) * kHPT;
+            const int r = (int)(lq * 32 + lane);
+            const uint32_t lane_base = (lq * 32u) << 16;
+            float* s_g = s_wmax;                              // g[h] = f_sp[h] / l[h] (free by now)
+            if (st < kH) {
+                const int h = st;
+                float ls[kMaxClusterMerge];
+                float mx = -INFINITY;
 #pragma unroll
                 for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
-                    const unsigned rk = (unsigned)min(s2, splits - 1);
-                    r_lse[s2] = cluster.map_shared_rank(s_l + 6 * kH, rk);
-                    r_o[s2] = cluster.map_shared_rank(reinterpret_cast<const float4*>(smem + kOffKV), rk);
+                    ls[s2] = s2 < splits ? *cluster.map_shared_rank(s_l + 6 * kH + h, (unsigned)s2) : -INFINITY;
+                    mx = fmaxf(mx, ls[s2]);
                 }
-                const int hs = kH / splits;
-                for (int item = st; item < hs * (kDV / 4); item += kSoftmaxThreads) {
-                    const int h = sp + splits * (item / (kDV / 4));
-                    const int d4 = item % (kDV / 4);
-                    float ls[kMaxClusterMerge];
-                    float mx = -INFINITY;
+                float wsum = 0.f;
 #pragma unroll
-                    for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
-                        ls[s2] = s2 < splits ? r_lse[s2][h] : -INFINITY;
-                        mx = fmaxf(mx, ls[s2]);
-                    }
-                    float wsum = 0.f;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (mx > -INFINITY) {
-#pragma unroll
-                        for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
-                            if (s2 >= splits || ls[s2] == -INFINITY) continue;
-                            const float wgt = expf(ls[s2] - mx);
-                            wsum += wgt;
-                            const float4 v = r_o[s2][h * (kDV / 4) + d4];
-                            acc.x = fmaf(wgt, v.x, acc.x);
-                            acc.y = fmaf(wgt, v.y, acc.y);
-                            acc.z = fmaf(wgt, v.z, acc.z);
-                            acc.w = fmaf(wgt, v.w, acc.w);
-                        }
-                    }
-                    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-                    uint2 pk;
-                    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2*>(out + (grow * kH + h) * kDV + 4 * d4) = pk;
-                    if (lse && d4 == 0) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
-                }
+                for (int s2 = 0; s2 < kMaxClusterMerge; ++s2)
+                    if (mx > -INFINITY && s2 < splits && ls[s2] != -INFINITY) wsum += expf(ls[s2] - mx);
+                const float f = wsum > 0.f && ls[sp] != -INFINITY ? expf(ls[sp] - mx) / wsum : 0.f;
+                s_g[h] = f * s_l[5 * kH + h];
+                if (lse && h % splits == sp) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
             }
+            named_bar_sync(1, kSoftmaxThreads);
+            // the head arithmetic below is specialised on the split count
+            // (2 or 4, a divisor of the 32 heads of a thread), so it folds
+            auto merge_heads = [&](auto splits_c) {
+                constexpr int S = decltype(splits_c)::value;
+                constexpr int hsS = kH / S;
+                constexpr uint32_t slotS = (uint32_t)(hsS * kDV * 2);
+                // this split's contribution to every other rank's heads, bf16,
+                // rank q's heads h = q + S k at [q][k][d] in the (free) row tile
+                tc_fence_after();
+                uint16_t* send = reinterpret_cast<uint16_t*>(smem + kOffKV);
+                for (int dv = 0; dv < 4; ++dv) {
+                    const int d = dv * 128 + r;
+                    uint32_t u[kHPT];
+                    if (nblk > 0) {
+                        tmem_ld_hpt(tmem + lane_base + kTmemO + dv * kH + h0, u);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < kHPT; ++x) u[x] = 0u;
+                    }
+#pragma unroll
+                    for (int x = 0; x < kHPT; ++x) {
+                        const int q = x % S;                   // h0 is a multiple of kHPT
+                        if (q == sp) continue;
+                        const int h = h0 + x;
+                        const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(u[x]) * s_g[h]);
+                        send[(q * hsS + h0 / S + x / S) * kDV + d] = *reinterpret_cast<const uint16_t*>(&b16);
+                    }
+                }
+                fence_proxy_async_smem();    // the generic-proxy stores, before the bulk copies read them
+                named_bar_sync(1, kSoftmaxThreads);
+                if (st == 0) {
+                    for (int q = 0; q < S; ++q) {
+                        if (q == sp) continue;
+                        const uint32_t dst =
+                            map_to_cluster_rank(smem_u32(smem + kOffQ) + (uint32_t)sp * slotS, (uint32_t)q);
+                        bulk_copy_to_peer(dst, smem_u32(smem + kOffKV) + (uint32_t)q * slotS, slotS,
+                                          map_to_cluster_rank(bar(kBarRecv), (uint32_t)q));
+                    }
+                }
+                // every other split's contribution to this rank's heads
+                const bool got = !named_bar_or(3, kSoftmaxThreads, !mbar_wait(bar(kBarRecv), 0));
+                if (!got) {
+                    latch_status(status, DSA_ERR_TIMEOUT);
+                    return;
+                }
+                const uint16_t* recv = reinterpret_cast<const uint16_t*>(smem + kOffQ);
+                tc_fence_after();
+                for (int dv = 0; dv < 4; ++dv) {
+                    const int d = dv * 128 + r;
+                    uint32_t u[kHPT];
+                    if (nblk > 0) {
+                        tmem_ld_hpt(tmem + lane_base + kTmemO + dv * kH + h0, u);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < kHPT; ++x) u[x] = 0u;
+                    }
+#pragma unroll
+                    for (int x = 0; x < kHPT; ++x) {
+                        if (x % S != sp) continue;
+                        const int h = h0 + x;
+                        const int k = h0 / S + x / S;
+                        float acc = 0.f;
+#pragma unroll
+                        for (int s2 = 0; s2 < S; ++s2) {
+                            const float c = s2 == sp ? __uint_as_float(u[x]) * s_g[h]
+                                                     : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                                           recv + (s2 * hsS + k) * kDV + d));
+                            acc += c;
+                        }
+                        const __nv_bfloat16 b16 = __float2bfloat16_rn(acc);
+                        out[(grow * kH + h) * kDV + d] = *reinterpret_cast<const uint16_t*>(&b16);
+                    }
+                }
+            };
+            if (splits == 2) merge_heads(std::integral_constant<int, 2>{});
+            else merge_heads(std::integral_constant<int, 4>{});
         }
-        cluster.sync();                                       // no partial is read after its CTA exits
+        // a CTA's row tile is the source of its bulk copies and its Q region
+        // their destination: none exits before every copy has landed
+        cluster.sync();
     }
 
     tc_fence_before();
