@@ -74,6 +74,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--kernel-reps", type=int, default=20)
     p.add_argument("--no-side", action="store_true", help="skip the prefill / long-decode sets of the default line")
+    p.add_argument("--clock-hold-s", type=float, default=0.5,
+                   help="seconds of untimed repeats after the timed steps, for clock samples (0: none)")
     return p.parse_args()
 
 
@@ -733,7 +735,7 @@ def run_dsa(args):
     # a short timed region holds few clock samples: repeat the same steps
     # for about half a second under the sampler (not timed)
     t_hold = time.time()
-    n_hold = max(1, int(0.5 / max(ms / K / 1e3, 1e-6)))
+    n_hold = int(args.clock_hold_s / max(ms / K / 1e3, 1e-6))
     for i in range(n_hold):
         case.step(i)
     barrier()

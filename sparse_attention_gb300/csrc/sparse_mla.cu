@@ -68,6 +68,7 @@ constexpr int kQChunkBytes = kH * 128;       // 8 KiB
 #define DSA_ATTN_SOFTMAX_WARPS 8
 #endif
 constexpr int kProducerWarps = DSA_ATTN_PRODUCER_WARPS;
+
 constexpr int kProducerRows = kBlk / (4 * kProducerWarps);   // rows of a block per producer lane
 constexpr int kMmaWarp = kProducerWarps;                  // warp 2
 constexpr int kSoftmaxWarp0 = kMmaWarp + 1;               // warps 3..10
@@ -110,9 +111,36 @@ constexpr int kBarRecv = kBarDrain + 1;                       // cluster merge: 
 constexpr int kNumBars = kBarRecv + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+// epilogue staging tiles (one per softmax warp, 32 rows x 32 columns of
+// fp32 at most) in the row tile, after the 64 KiB a cluster merge sends from
+constexpr int kStageOff = 65536;
+constexpr int kStageBytes = 32 * 32 * 4;
+static_assert(kStageOff + kSoftmaxWarps * kStageBytes <= kChunks * kKVChunkBytes, "staging fits in the row tile");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;                                // O^T: 4 blocks x 64 columns
 constexpr uint32_t kTmemS = 256;                              // S^T: 64 columns
+
+// A warp's results for NX rows of a row-major destination, one column per
+// lane (columns d0 .. d0 + 31 of row x at dst + x * row_stride): staged in
+// the warp's own shared-memory tile, then written back with 16-byte stores
+// (a 2-byte store per lane and row cost ~16 cycles per warp instruction).
+// dst and row_stride keep every row 16-byte aligned.
+template <typename T, int NX>
+__device__ __forceinline__ void store_warp_tile(T* stage, const T (&v)[NX], T* dst, int64_t row_stride,
+                                                uint32_t lane) {
+#pragma unroll
+    for (int x = 0; x < NX; ++x) stage[x * 32 + lane] = v[x];
+    __syncwarp();
+    constexpr int kVec = 16 / (int)sizeof(T);         // elements per 16 bytes
+    constexpr int kPerRow = 32 / kVec;                // 16-byte pieces of a row's 32 columns
+#pragma unroll
+    for (int c = (int)lane; c < NX * kPerRow; c += 32) {
+        const int x = c / kPerRow, q = c % kPerRow;
+        *reinterpret_cast<uint4*>(dst + x * row_stride + q * kVec) =
+            *reinterpret_cast<const uint4*>(stage + x * 32 + q * kVec);
+    }
+    __syncwarp();
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_tc_kernel(const BatchDev bd, const RowRange rr, const __grid_constant__ CUtensorMap tm_q,
@@ -400,35 +428,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph = (uint32_t)jb & 1u;
             const bool got = !misc[1] && mbar_wait(bar(kBarIdx + (jb & 1)), ((uint32_t)jb >> 1) & 1u) &&
                              mbar_wait(bar(kBarS), ph);
-            // every abort is agreed by all softmax threads before any named
-            // barrier, so none of them can be left waiting at one
-            if (named_bar_or(3, kSoftmaxThreads, !got)) {
-                ok = false;
-                break;
-            }
             tc_fence_after();
             const bool valid = s_idx[(jb & 1) * kBlk + r] >= 0;
+            // the running max moves only when a score exceeds it by 2^8; the
+            // vote compares raw scores with (m + 8) / c2 per head (a trigger
+            // only: the exact block max below decides whether m moves).  The
+            // bounds are read while the TMEM load is in flight.
             float s[kHPT];
+            bool exceed = false;
             {
                 uint32_t u[kHPT];
                 tmem_ld_hpt(tmem + lane_base + kTmemS + h0, u);
+                float4 tv[kHPT / 4];
+#pragma unroll
+                for (int x = 0; x < kHPT; x += 4) tv[x / 4] = *reinterpret_cast<const float4*>(s_thr + h0 + x);
                 tmem_ld_wait();
 #pragma unroll
                 for (int x = 0; x < kHPT; ++x) s[x] = valid ? __uint_as_float(u[x]) : -INFINITY;
-            }
-            // the running max moves only when a score exceeds it by 2^8; the
-            // vote compares raw scores with (m + 8) / c2 per head (a trigger
-            // only: the exact block max below decides whether m moves)
-            bool exceed = false;
 #pragma unroll
-            for (int x = 0; x < kHPT; x += 4) {
-                const float4 tv = *reinterpret_cast<const float4*>(s_thr + h0 + x);
-                exceed |= s[x] > tv.x;
-                exceed |= s[x + 1] > tv.y;
-                exceed |= s[x + 2] > tv.z;
-                exceed |= s[x + 3] > tv.w;
+                for (int x = 0; x < kHPT; x += 4) {
+                    exceed |= s[x] > tv[x / 4].x;
+                    exceed |= s[x + 1] > tv[x / 4].y;
+                    exceed |= s[x + 2] > tv[x / 4].z;
+                    exceed |= s[x + 3] > tv[x / 4].w;
+                }
             }
-            if (named_bar_or(2, kSoftmaxThreads, exceed)) {
+            // a thread whose wait failed (abort or time-out) joins the vote
+            // with the slow path, where every softmax thread learns of it
+            // after the same barrier and all stop together: no named barrier
+            // is ever left waiting
+            if (named_bar_or(2, kSoftmaxThreads, exceed || !got)) {
+                volatile int* s_abort = reinterpret_cast<volatile int*>(s_l);   // [softmax warp], unused until the epilogue
+                const bool wabort = __any_sync(0xffffffffu, !got);
+                if (lane == 0) s_abort[warp - kSoftmaxWarp0] = wabort ? 1 : 0;
                 // exact per-head block max: warp max, then across lane quarters
 #pragma unroll
                 for (int x = 0; x < kHPT; ++x) {
@@ -436,6 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) s_wmax[lq * kH + h0 + x] = mx;
                 }
                 named_bar_sync(1, kSoftmaxThreads);
+                bool any_abort = false;
+#pragma unroll
+                for (int w2 = 0; w2 < kSoftmaxWarps; ++w2) any_abort |= s_abort[w2] != 0;
+                if (any_abort) {
+                    ok = false;
+                    break;
+                }
                 bool need = false;
                 if (st < kH) {
                     const float mb = fmaxf(fmaxf(s_wmax[st], s_wmax[kH + st]),
@@ -551,10 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 inv[x + 2] = v.z;
                 inv[x + 3] = v.w;
             }
-            uint16_t* ob = out + (grow * kH + h0) * kDV;
-            float* po = splits > 1 ? part_o + (prow * kH + h0) * kDV : nullptr;
+            // the warp's staging tile: the row tile is free once every PV is done
+            uint8_t* stage = smem + kOffKV + kStageOff + (warp - kSoftmaxWarp0) * kStageBytes;
             for (int dv = 0; dv < 4; ++dv) {
-                const int d = dv * 128 + r;                   // output column of this thread
+                const int d0 = dv * 128 + (int)(lq * 32);      // the warp's 32 output columns
                 uint32_t u[kHPT];
                 if (nblk > 0) {
                     tmem_ld_hpt(tmem + lane_base + kTmemO + dv * kH + h0, u);
@@ -563,15 +602,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int x = 0; x < kHPT; ++x) u[x] = 0u;
                 }
+                if (splits == 1) {
+                    uint16_t o16[kHPT];
 #pragma unroll
-                for (int x = 0; x < kHPT; ++x) {
-                    const float o = __uint_as_float(u[x]) * inv[x];
-                    if (splits == 1) {
-                        const __nv_bfloat16 b16 = __float2bfloat16_rn(o);
-                        ob[x * kDV + d] = *reinterpret_cast<const uint16_t*>(&b16);
-                    } else {
-                        po[x * kDV + d] = o;
+                    for (int x = 0; x < kHPT; ++x) {
+                        const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(u[x]) * inv[x]);
+                        o16[x] = *reinterpret_cast<const uint16_t*>(&b16);
                     }
+                    store_warp_tile(reinterpret_cast<uint16_t*>(stage), o16, out + (grow * kH + h0) * kDV + d0,
+                                    kDV, lane);
+                } else {
+                    float o32[kHPT];
+#pragma unroll
+                    for (int x = 0; x < kHPT; ++x) o32[x] = __uint_as_float(u[x]) * inv[x];
+                    store_warp_tile(reinterpret_cast<float*>(stage), o32, part_o + (prow * kH + h0) * kDV + d0,
+                                    kDV, lane);
                 }
             }
         }
@@ -662,6 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint16_t* recv = reinterpret_cast<const uint16_t*>(smem + kOffQ);
                 tc_fence_after();
+                uint16_t* stage =
+                    reinterpret_cast<uint16_t*>(smem + kOffKV + kStageOff + (warp - kSoftmaxWarp0) * kStageBytes);
                 for (int dv = 0; dv < 4; ++dv) {
                     const int d = dv * 128 + r;
                     uint32_t u[kHPT];
@@ -672,22 +719,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int x = 0; x < kHPT; ++x) u[x] = 0u;
                     }
+                    // this rank's heads of the thread: x = sp + S j
+                    uint16_t o16[kHPT / S];
 #pragma unroll
-                    for (int x = 0; x < kHPT; ++x) {
-                        if (x % S != sp) continue;
-                        const int h = h0 + x;
-                        const int k = h0 / S + x / S;
+                    for (int j = 0; j < kHPT / S; ++j) {
+                        const int h = h0 + sp + S * j;
+                        const int k = h0 / S + j;
+                        // u[sp + S j] with sp < S chosen by selects (no local-memory indexing)
+                        uint32_t uv = u[S * j];
+#pragma unroll
+                        for (int q = 1; q < S; ++q)
+                            if (sp == q) uv = u[S * j + q];
                         float acc = 0.f;
 #pragma unroll
                         for (int s2 = 0; s2 < S; ++s2) {
-                            const float c = s2 == sp ? __uint_as_float(u[x]) * s_g[h]
+                            const float c = s2 == sp ? __uint_as_float(uv) * s_g[h]
                                                      : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
                                                            recv + (s2 * hsS + k) * kDV + d));
                             acc += c;
                         }
                         const __nv_bfloat16 b16 = __float2bfloat16_rn(acc);
-                        out[(grow * kH + h) * kDV + d] = *reinterpret_cast<const uint16_t*>(&b16);
+                        o16[j] = *reinterpret_cast<const uint16_t*>(&b16);
                     }
+                    store_warp_tile(stage, o16, out + (grow * kH + h0 + sp) * kDV + dv * 128 + (int)(lq * 32),
+                                    (int64_t)S * kDV, lane);
                 }
             };
             if (splits == 2) merge_heads(std::integral_constant<int, 2>{});
