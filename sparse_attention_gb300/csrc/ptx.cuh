@@ -151,6 +151,14 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t
         : "memory");
 }
 
+// One arrival, with release semantics at cluster scope, on an mbarrier in a
+// cluster peer's shared memory (`bar_cluster` from map_to_cluster_rank): the
+// peer that waits on it sees this thread's earlier writes and the completion
+// of everything this thread waited for before arriving.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
