@@ -110,34 +110,33 @@ constexpr int kBarP = kBarS + 1;                              // P^T written (on
 constexpr int kBarO = kBarP + 1;                              // PV of a block done (chunk 8 free)
 constexpr int kBarIdx = kBarO + 1;                            // [2]: indices of a block published
 constexpr int kBarDrain = kBarIdx + 2;
-constexpr int kBarRecv = kBarDrain + 1;                       // cluster merge: the peers' contributions landed
+constexpr int kBarRecv = kBarDrain + 1;                       // cluster merge: the peers' pieces landed
 constexpr int kBarInfo = kBarRecv + 1;                        // [2]: an item's block count published
 constexpr int kBarOFree = kBarInfo + 2;                       // an item's output read out of TMEM (one arrival per softmax warp)
 constexpr int kBarSlotFree = kBarOFree + 1;                   // [2]: an info slot read (the MMA thread + one per softmax warp)
 constexpr int kBarPeerFree = kBarSlotFree + 2;                 // cluster merge: every peer's Q region may be written
-constexpr int kNumBars = kBarPeerFree + 1;
+constexpr int kBarRecvLse = kBarPeerFree + 1;                  // cluster merge: the peers' lse landed
+constexpr int kNumBars = kBarRecvLse + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-// epilogue staging tiles (one per softmax warp, 32 rows x 32 columns of
-// fp32 at most) in the row tile, after the 64 KiB a cluster merge sends from
-constexpr int kStageOff = 65536;
-constexpr int kStageBytes = 32 * 32 * 4;
-static_assert(kStageOff + kSoftmaxWarps * kStageBytes <= kChunks * kKVChunkBytes, "staging fits in the row tile");
 // Cluster merge of a row's S = 2 or 4 splits (cluster rank = split).  A
 // piece is what one softmax warp sends one peer for one 128-column block dv
 // of O: the peer's kHPT / S heads of the warp's head group at the warp's 32
-// columns, bf16 pairs of heads [j / 2][lane][j % 2]; a rank's pieces are
-// [dv][softmax warp], S x 4 x 8 x (32 / S) x 64 bytes = 64 KiB for all ranks.
-// The send slots (one per receiving rank) fill the row tile below the
-// staging tiles, the receive slots (one per sending rank) the Q region; the
-// senders' lse follow.
-constexpr int kMergeSlotsBytes = 65536;
-constexpr int kMergeLseSend = kStageOff + kSoftmaxWarps * kStageBytes;   // row tile: this rank's lse [64]
+// columns, bf16 pairs of heads [j / 2][lane][j % 2], (32 / S) x 64 bytes.
+// Sent from row-tile chunk 2 dv, which the last PV of block dv has just
+// freed: [receiving rank][softmax warp] pieces, 16 KiB for every S.  Received
+// into the Q region, free once the rank's last S^T is done: [sending rank]
+// [dv][softmax warp] pieces, 64 KiB, then the senders' lse [rank][64].  The
+// merge's output staging tiles (one per softmax warp, 32 x 32 bf16) sit in
+// chunks 1 and 3, free by then.
+constexpr int kMergeSlotsBytes = 65536;                                  // receive slots of all ranks
 constexpr int kMergeLseRecv = kMergeSlotsBytes;                          // Q region: [sending rank][64] lse
+constexpr int kStageBytes = 32 * 32 * 2;
+static_assert(kSoftmaxWarps * kHPT * 64 <= kKVChunkBytes, "a block's pieces (S x 8 x (32 / S) x 64 bytes) fit a chunk");
 static_assert(4 * kSoftmaxWarps * kHPT * 64 == kMergeSlotsBytes, "merge slots");
-static_assert(kMergeSlotsBytes <= kStageOff, "send slots below the staging tiles");
-static_assert(kMergeLseSend + kH * 4 <= kChunks * kKVChunkBytes, "lse send area in the row tile");
+static_assert(kSoftmaxWarps / 2 * kStageBytes <= kKVChunkBytes, "half the staging tiles fit a chunk");
 static_assert(kMergeLseRecv + kMaxClusterMerge * kH * 4 <= kChunks * kQChunkBytes, "receive slots in the Q region");
+static_assert(kOffL % 16 == 0 && (6 * kH * 4) % 16 == 0, "the lse of s_l is a bulk copy source");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;                                // O^T: 4 blocks x 64 columns
 constexpr uint32_t kTmemS = 256;                              // S^T: 64 columns
@@ -184,6 +183,182 @@ __device__ __forceinline__ void store_warp_tile(T* stage, const T (&v)[NX], T* d
             *reinterpret_cast<const uint4*>(stage + x * 32 + q * kVec);
     }
     __syncwarp();
+}
+
+// The merge of a row's S = 2 or 4 splits inside their cluster (rank =
+// split), run by the softmax warps of every rank once the split's l and lse
+// (s_l) and its output O^T (TMEM) are final.  Rank sp writes the heads
+// h = sp (mod S):
+//   out[h] = sum_s f_s[h] o_s[h] / l_s[h],
+//   f_s = exp(lse_s - m) / sum_s' exp(lse_s' - m),  m = max_s lse_s,
+// o_s / l_s the split's normalised output.  Each warp sends every peer its
+// heads of the warp's 32 columns, normalised, in bf16, one piece per
+// 128-column block as soon as it is converted (distributed shared memory
+// moves ~14 bytes per clock); a rank's own term is read again from TMEM, in
+// fp32.  The weights need every split's lse, which travels ahead of the
+// pieces.
+//
+// Its loops stay rolled: this code runs once per CTA, from a cold
+// instruction cache.
+template <int S>
+__device__ __forceinline__ void cluster_merge_tail(uint8_t* smem, const uint32_t tmem, const int sp, const int nblk,
+                                                   const uint32_t last_ph, const int64_t grow,
+                                                   uint16_t* __restrict__ out, float* __restrict__ lse,
+                                                   int32_t* status) {
+    constexpr int hq = kHPT / S;                          // a warp's heads of one rank
+    constexpr uint32_t kPiece = (uint32_t)hq * 32u * 2u;
+    constexpr uint32_t kSlot = (uint32_t)kMergeSlotsBytes / S;
+    const uint32_t warp = warp_id(), lane = lane_id();
+    const uint32_t lq = warp & 3u;
+    const uint32_t wl = warp - kSoftmaxWarp0;
+    const int h0 = ((int)wl >> 2) * kHPT;
+    const int st = (int)threadIdx.x - 32 * kSoftmaxWarp0;
+    const uint32_t lane_base = (lq * 32u) << 16;
+    const float* s_l = reinterpret_cast<const float*>(smem + kOffL);
+    float* s_f = reinterpret_cast<float*>(smem + kOffWmax);      // f_s[h] at [s][h] (block-max scratch)
+    const uint32_t bar0 = smem_u32(smem + kOffBar);
+    auto bar = [&](int n) { return bar0 + 8u * (uint32_t)n; };
+    const uint32_t sQr = smem_u32(smem + kOffQ);
+    // a peer's Q region is free once its MMAs have drained
+    const bool peers_free = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar(kBarPeerFree), 0) : false, 0);
+    if (st == 0 && peers_free) {
+        for (int q = 0; q < S; ++q)
+            if (q != sp)
+                bulk_copy_to_peer(map_to_cluster_rank(sQr + kMergeLseRecv + (uint32_t)sp * kH * 4, (uint32_t)q),
+                                  smem_u32(smem + kOffL + 6 * kH * 4), kH * 4,
+                                  map_to_cluster_rank(bar(kBarRecvLse), (uint32_t)q));
+    }
+    float inv[kHPT];                                      // 1 / l of this thread's heads
+#pragma unroll
+    for (int x = 0; x < kHPT; x += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(s_l + 5 * kH + h0 + x);
+        inv[x] = v.x;
+        inv[x + 1] = v.y;
+        inv[x + 2] = v.z;
+        inv[x + 3] = v.w;
+    }
+#pragma unroll 1
+    for (int dv = 0; dv < 4; ++dv) {
+        uint32_t u[kHPT];
+        if (nblk > 0) {
+            // this 128-column block of O^T is final once the last block's PV
+            // has written it (last_ph: that block's phase)
+            if (!mbar_wait(bar(kBarPair + dv), last_ph)) latch_status(status, DSA_ERR_TIMEOUT);
+            tc_fence_after();
+            tmem_ld_hpt(tmem + lane_base + kTmemO + dv * kH + h0, u);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int x = 0; x < kHPT; ++x) u[x] = 0u;
+        }
+        const uint32_t poff = ((uint32_t)dv * kSoftmaxWarps + wl) * kPiece;     // in a receive slot
+        const uint32_t soff = (uint32_t)(2 * dv * kKVChunkBytes) + wl * kPiece;  // + q 8 kPiece: in the row tile
+#pragma unroll
+        for (int q = 0; q < S; ++q) {
+            uint32_t* piece = reinterpret_cast<uint32_t*>(smem + kOffKV + soff + q * kSoftmaxWarps * kPiece);
+#pragma unroll
+            for (int j = 0; j < hq; j += 2) {
+                const float va = __uint_as_float(u[q + S * j]) * inv[q + S * j];
+                const float vb = __uint_as_float(u[q + S * (j + 1)]) * inv[q + S * (j + 1)];
+                if (q != sp) piece[(j / 2) * 32 + lane] = pack_bf16x2(va, vb);
+            }
+        }
+        fence_proxy_async_smem();      // the generic-proxy stores, before the bulk copies read them
+        __syncwarp();
+        if (lane == 0 && peers_free) {
+            for (int q = 0; q < S; ++q)
+                if (q != sp)
+                    bulk_copy_to_peer(map_to_cluster_rank(sQr + (uint32_t)sp * kSlot + poff, (uint32_t)q),
+                                      smem_u32(smem + kOffKV) + soff + (uint32_t)q * kSoftmaxWarps * kPiece,
+                                      kPiece, map_to_cluster_rank(bar(kBarRecv), (uint32_t)q));
+        }
+    }
+    // the weights, from every split's lse, while the pieces are in flight
+    // (every wait below is agreed by all softmax threads)
+    const bool got_lse = !named_bar_or(3, kSoftmaxThreads, !peers_free || !mbar_wait(bar(kBarRecvLse), 0));
+    if (got_lse && st < kH) {
+        const int h = st;
+        const float* rl = reinterpret_cast<const float*>(smem + kOffQ + kMergeLseRecv);
+        float ls[S];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) {
+            ls[s2] = s2 == sp ? s_l[6 * kH + h] : rl[s2 * kH + h];
+            mx = fmaxf(mx, ls[s2]);
+        }
+        float wsum = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2)
+            if (mx > -INFINITY && ls[s2] != -INFINITY) wsum += expf(ls[s2] - mx);
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2)
+            s_f[s2 * kH + h] = wsum > 0.f && ls[s2] != -INFINITY ? expf(ls[s2] - mx) / wsum : 0.f;
+        if (lse && h % S == sp) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+    }
+    // every peer's pieces have landed
+    const bool got = got_lse && !named_bar_or(3, kSoftmaxThreads, !mbar_wait(bar(kBarRecv), 0));
+    if (!got) {
+        latch_status(status, DSA_ERR_TIMEOUT);
+        return;
+    }
+    uint16_t* stage = reinterpret_cast<uint16_t*>(smem + kOffKV + (2 * (wl / 4) + 1) * kKVChunkBytes +
+                                                  (wl % 4) * kStageBytes);
+    // the weights of this thread's heads h0 + sp + S j, every split
+    float fw[hq][S];
+#pragma unroll
+    for (int j = 0; j < hq; ++j)
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) fw[j][s2] = s_f[s2 * kH + h0 + sp + S * j];
+    tc_fence_after();
+#pragma unroll 1
+    for (int dv = 0; dv < 4; ++dv) {
+        const uint32_t poff = ((uint32_t)dv * kSoftmaxWarps + wl) * kPiece;
+        uint32_t u[kHPT];
+        if (nblk > 0) {
+            tmem_ld_hpt(tmem + lane_base + kTmemO + dv * kH + h0, u);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int x = 0; x < kHPT; ++x) u[x] = 0u;
+        }
+        uint16_t o16[hq];
+#pragma unroll
+        for (int j = 0; j < hq; j += 2) {
+            // in split order, this rank's term at its place
+            float acc_a = 0.f, acc_b = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < S; ++s2) {
+                float va, vb;
+                if (s2 == sp) {
+                    // u[sp + S j] with sp < S chosen by selects (no local-memory indexing)
+                    uint32_t ua = u[S * j], ub = u[S * (j + 1)];
+                    float ia = inv[S * j], ib = inv[S * (j + 1)];
+#pragma unroll
+                    for (int q = 1; q < S; ++q)
+                        if (sp == q) {
+                            ua = u[S * j + q];
+                            ub = u[S * (j + 1) + q];
+                            ia = inv[S * j + q];
+                            ib = inv[S * (j + 1) + q];
+                        }
+                    va = __uint_as_float(ua) * ia;
+                    vb = __uint_as_float(ub) * ib;
+                } else {
+                    const uint32_t w2 =
+                        reinterpret_cast<const uint32_t*>(smem + kOffQ + s2 * kSlot + poff)[(j / 2) * 32 + lane];
+                    va = __uint_as_float(w2 << 16);
+                    vb = __uint_as_float(w2 & 0xFFFF0000u);
+                }
+                acc_a = fmaf(fw[j][s2], va, acc_a);
+                acc_b = fmaf(fw[j + 1][s2], vb, acc_b);
+            }
+            const __nv_bfloat16 ba = __float2bfloat16_rn(acc_a), bb = __float2bfloat16_rn(acc_b);
+            o16[j] = *reinterpret_cast<const uint16_t*>(&ba);
+            o16[j + 1] = *reinterpret_cast<const uint16_t*>(&bb);
+        }
+        store_warp_tile(stage, o16, out + (grow * kH + h0 + sp) * kDV + dv * 128 + (int)(lq * 32),
+                        (int64_t)S * kDV, lane);
+    }
 }
 
 // What a CTA writes for its items.  Each kernel instance holds the code of
@@ -265,6 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before the top-k started.
     Item first;
     const bool first_ok = (int64_t)blockIdx.x < n_items && item_at(blockIdx.x, first);
+    auto get_item = [&](int64_t it, Item& o) -> bool {
+        if (it != (int64_t)blockIdx.x) return item_at(it, o);
+        o = first;
+        return first_ok;
+    };
     if (threadIdx.x == 32 * kMmaWarp) prefetch_tmap(&tm_q);
     if (threadIdx.x == 0) {
         for (int n = 0; n < kNumBars; ++n) {
@@ -277,8 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // a row merged in a cluster receives, from every other split, its
         // slot of pieces and its lse
-        if constexpr (kCluster)
-            mbar_arrive_expect_tx(bar(kBarRecv), (uint32_t)((kMode - 1) * (kMergeSlotsBytes / kMode + kH * 4)));
+        if constexpr (kCluster) {
+            mbar_arrive_expect_tx(bar(kBarRecv), (uint32_t)((kMode - 1) * (kMergeSlotsBytes / kMode)));
+            mbar_arrive_expect_tx(bar(kBarRecvLse), (uint32_t)((kMode - 1) * kH * 4));
+        }
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -314,17 +496,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t nitem = 0;      // items so far: the info slot and the phases of per-item barriers
         for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
             Item I;
-            if (!item_at(it, I)) continue;
+            if (!get_item(it, I)) continue;
             const uint8_t* kv_seq = reinterpret_cast<const uint8_t*>(kv) + (int64_t)I.b * bd.stride * (kDQK * 2);
             // blocks of this segment: up to its last valid entry (16-byte
             // loads when the rows are 16-byte aligned, one round trip); with
-            // L2 prefetching on, the rows of the first block are prefetched
-            // as their indices are seen
+            // L2 prefetching on, the rows of the first 1 + kPrefetchAhead
+            // blocks are prefetched as their indices are seen
             auto prefetch_row = [&](int j, int32_t sv) {
-                if (l2_prefetch && j < I.j_begin + kPrefetchAhead * kBlk && sv >= 0 && sv <= I.t)
+                if (l2_prefetch && j < I.j_begin + (1 + kPrefetchAhead) * kBlk && sv >= 0 && sv <= I.t)
                     prefetch_l2_bulk(kv_seq + (int64_t)sv * (kDQK * 2), kDQK * 2);
             };
             int last = -1;
+            // with 16-byte loads, lane l of warp 0 holds entries 4l .. 4l + 3
+            // of the first block: they go to shared memory from registers
+            int4 blk0 = make_int4(-1, -1, -1, -1);
+            const bool blk0_in_regs = (k & 3) == 0;
             if ((k & 3) == 0) {
                 // at most kMaxTopk / 4 groups of four indices: every group of
                 // this thread is loaded before any is tested (one round trip)
@@ -337,6 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int q = gl + u * kPT;
                     vs[u] = q < nq4 ? __ldg(sel4 + q) : make_int4(-1, -1, -1, -1);
                 }
+                blk0 = vs[0];
+                static_assert(kPT >= 32 && kBlk == 4 * 32, "warp 0's first loads cover the first block");
 #pragma unroll
                 for (int u = 0; u < kScanIt; ++u) {
                     const int q = gl + u * kPT;
@@ -383,16 +571,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ph = gb & 1u;
                 int32_t* ib = s_idx + (gb & 1u) * kBlk;
                 // this block's indices (warp 0) are loaded before the prefetch
-                // below, so that the two round trips overlap
-                int32_t v[4];
-                if (warp == 0) {
+                // below, so that the two round trips overlap; the first
+                // block's come from the scan (entry 4 lane + u in v[u], else
+                // entry 32 u + lane)
+                const bool from_scan = jb == 0 && blk0_in_regs;
+                int32_t v[4] = {blk0.x, blk0.y, blk0.z, blk0.w};
+                if (warp == 0 && !from_scan) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int j = I.j_begin + jb * kBlk + u * 32 + (int)lane;
                         v[u] = (j < I.j_end) ? __ldg(I.sel + j) : -1;
                     }
                 }
-                if (l2_prefetch && jb + kPrefetchAhead < nblk) {
+                // (the scan prefetched the blocks up to kPrefetchAhead)
+                if (l2_prefetch && jb > 0 && jb + kPrefetchAhead < nblk) {
                     // the rows of block jb + kPrefetchAhead (valid indices only),
                     // one 1152-byte bulk prefetch each
                     for (int u = gl; u < kBlk; u += kPT) {
@@ -417,8 +609,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // block's indices and row offsets are ready before PV(gb - 1)
                     const bool wok2 = __all_sync(0xffffffffu, !misc[1]);
                     if (wok2) {
+                        if (from_scan) {
+                            reinterpret_cast<int4*>(ib)[lane] = make_int4(v[0], v[1], v[2], v[3]);
+                        } else {
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) ib[u * 32 + lane] = v[u];
+                            for (int u = 0; u < 4; ++u) ib[u * 32 + lane] = v[u];
+                        }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(kBarIdx + (gb & 1u)));
                     } else {
@@ -478,9 +674,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true, q_pending = false;
             uint32_t gb = 0, nitem = 0, nq = 0;
             int my_sp = 0;
+            bool peers_told = false;
+            // the peers of a cluster may send into this CTA's Q region once
+            // nothing reads it any more
+            auto tell_peers = [&]() {
+                if constexpr (kCluster) {
+                    for (int q = 0; q < kMode; ++q)
+                        if (q != my_sp) mbar_arrive_peer(map_to_cluster_rank(bar(kBarPeerFree), (uint32_t)q));
+                    peers_told = true;
+                }
+            };
             for (int64_t it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 Item I;
-                if (!item_at(it, I)) continue;
+                if (!get_item(it, I)) continue;
                 had_item = true;
                 my_sp = I.sp;
                 // Q of this item by TMA, once the S^T of the previous item's
@@ -536,6 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    // P^T of the last block is written, so its S^T, the last
+                    // reader of Q, has completed
+                    if (kCluster && jb == nblk - 1) tell_peers();
                     const uint32_t sP = sKV + kVChunks * kKVChunkBytes;
                     for (int dv = 0; dv < 4; ++dv) {
 #pragma unroll
@@ -559,13 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(kBarDrain));
             mbar_wait(bar(kBarDrain), 0);
             if (q_pending) mbar_wait(bar(kBarQ), nq & 1u);    // Q's copy must land before the CTA exits
-            if constexpr (kCluster) {
-                // nothing reads this CTA's Q region any more: the peers may
-                // send their pieces into it
-                if (had_item)
-                    for (int q = 0; q < kMode; ++q)
-                        if (q != my_sp) mbar_arrive_peer(map_to_cluster_rank(bar(kBarPeerFree), (uint32_t)q));
-            }
+            if (had_item && !peers_told) tell_peers();      // (no blocks, or an abort)
         }
         __syncwarp();
     } else {
@@ -581,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t gb = 0, nitem = 0;
         for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
             Item I;
-            if (!item_at(it, I)) continue;
+            if (!get_item(it, I)) continue;
             had_item = true;
             float lsum[kHPT];
 #pragma unroll
@@ -763,11 +966,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // x of a warp ends with head h0 + x of its lane quarter)
             static_assert(kHPT == 32, "one head per lane in the l reduction");
             s_l[lq * kH + h0 + lane] = warp_sum_scatter32(lsum, lane);
-            const bool got_o = nblk == 0 || mbar_wait(bar(kBarO), (gb - 1u) & 1u);
-            // agreed by every softmax thread: the stores below end with a barrier
-            if (named_bar_or(3, kSoftmaxThreads, !got_o)) {
-                ok = false;
-                break;
+            if constexpr (kCluster) {
+                // (the merge waits for each 128-column block of the last PV)
+                named_bar_sync(1, kSoftmaxThreads);
+            } else {
+                const bool got_o = nblk == 0 || mbar_wait(bar(kBarO), (gb - 1u) & 1u);
+                // agreed by every softmax thread: the stores below end with a barrier
+                if (named_bar_or(3, kSoftmaxThreads, !got_o)) {
+                    ok = false;
+                    break;
+                }
             }
             if (st < kH) {
                 const float lt = s_l[st] + s_l[kH + st] + s_l[2 * kH + st] + s_l[3 * kH + st];
@@ -778,10 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lse) lse[I.grow * kH + st] = ls;
                 } else if constexpr (kCluster) {
                     s_l[6 * kH + st] = ls;
-                    // sent to the peers by bulk copy (the row tile is free:
-                    // the last PV has completed)
-                    reinterpret_cast<float*>(smem + kOffKV + kMergeLseSend)[st] = ls;
-                    fence_proxy_async_smem();
+                    fence_proxy_async_smem();      // sent to the peers from s_l by bulk copy
                 } else {
                     part_lse[I.prow * kH + st] = ls;
                 }
@@ -838,158 +1043,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             misc[1] = 1;
         }
         if constexpr (kCluster) {
-            if (ok && had_item) {
-                // The row's splits are the CTAs of this cluster, rank = split;
-                // rank sp writes the heads h = sp (mod S):
-                //   out[h] = sum_s f_s[h] o_s[h] / l_s[h],
-                //   f_s = exp(lse_s - m) / sum_s' exp(lse_s' - m),  m = max_s lse_s,
-                // o_s / l_s the split's normalised output.  Each warp sends every
-                // peer its heads of the warp's 32 columns, normalised, in bf16,
-                // one piece per 128-column block as soon as it is converted
-                // (distributed shared memory moves ~14 bytes per clock); a
-                // rank's own term is read again from TMEM, in fp32.  The
-                // weights need every split's lse, which travels with the
-                // pieces.  The loops over dv stay rolled: this code runs once
-                // per CTA, from a cold instruction cache.
-                constexpr int S = kMode;
-                constexpr int hq = kHPT / S;                          // a warp's heads of one rank
-                constexpr uint32_t kPiece = (uint32_t)hq * 32u * 2u;
-                constexpr uint32_t kSlot = (uint32_t)kMergeSlotsBytes / S;
-                const int sp = c_sp;
-                const int nblk = c_nblk;
-                const uint32_t wl = warp - kSoftmaxWarp0;
-                const uint32_t sQr = smem_u32(smem + kOffQ);
-                // a peer's Q region is free once its MMAs have drained
-                const bool peers_free = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar(kBarPeerFree), 0) : false, 0);
-                if (st == 0 && peers_free) {
-                    for (int q = 0; q < S; ++q)
-                        if (q != sp)
-                            bulk_copy_to_peer(map_to_cluster_rank(sQr + kMergeLseRecv + (uint32_t)sp * kH * 4, (uint32_t)q),
-                                              smem_u32(smem + kOffKV + kMergeLseSend), kH * 4,
-                                              map_to_cluster_rank(bar(kBarRecv), (uint32_t)q));
-                }
-                float inv[kHPT];                                      // 1 / l of this thread's heads
-#pragma unroll
-                for (int x = 0; x < kHPT; x += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(s_l + 5 * kH + h0 + x);
-                    inv[x] = v.x;
-                    inv[x + 1] = v.y;
-                    inv[x + 2] = v.z;
-                    inv[x + 3] = v.w;
-                }
-                tc_fence_after();
-#pragma unroll 1
-                for (int dv = 0; dv < 4; ++dv) {
-                    uint32_t u[kHPT];
-                    if (nblk > 0) {
-                        tmem_ld_hpt(tmem + lane_base + kTmemO + dv * kH + h0, u);
-                        tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int x = 0; x < kHPT; ++x) u[x] = 0u;
-                    }
-                    const uint32_t poff = ((uint32_t)dv * kSoftmaxWarps + wl) * kPiece;
-#pragma unroll
-                    for (int q = 0; q < S; ++q) {
-                        uint32_t* piece = reinterpret_cast<uint32_t*>(smem + kOffKV + q * kSlot + poff);
-#pragma unroll
-                        for (int j = 0; j < hq; j += 2) {
-                            const float va = __uint_as_float(u[q + S * j]) * inv[q + S * j];
-                            const float vb = __uint_as_float(u[q + S * (j + 1)]) * inv[q + S * (j + 1)];
-                            if (q != sp) piece[(j / 2) * 32 + lane] = pack_bf16x2(va, vb);
-                        }
-                    }
-                    fence_proxy_async_smem();      // the generic-proxy stores, before the bulk copies read them
-                    __syncwarp();
-                    if (lane == 0 && peers_free) {
-                        for (int q = 0; q < S; ++q)
-                            if (q != sp)
-                                bulk_copy_to_peer(map_to_cluster_rank(sQr + (uint32_t)sp * kSlot + poff, (uint32_t)q),
-                                                  smem_u32(smem + kOffKV) + (uint32_t)q * kSlot + poff, kPiece,
-                                                  map_to_cluster_rank(bar(kBarRecv), (uint32_t)q));
-                    }
-                }
-                // every peer's pieces and lse have landed
-                const bool got = !named_bar_or(3, kSoftmaxThreads, !peers_free || !mbar_wait(bar(kBarRecv), 0));
-                if (!got) {
-                    latch_status(status, DSA_ERR_TIMEOUT);
-                } else {
-                    float* s_f = s_wmax;                              // f_s[h] at [s][h] (free by now)
-                    if (st < kH) {
-                        const int h = st;
-                        const float* rl = reinterpret_cast<const float*>(smem + kOffQ + kMergeLseRecv);
-                        float ls[S];
-                        float mx = -INFINITY;
-#pragma unroll
-                        for (int s2 = 0; s2 < S; ++s2) {
-                            ls[s2] = s2 == sp ? s_l[6 * kH + h] : rl[s2 * kH + h];
-                            mx = fmaxf(mx, ls[s2]);
-                        }
-                        float wsum = 0.f;
-#pragma unroll
-                        for (int s2 = 0; s2 < S; ++s2)
-                            if (mx > -INFINITY && ls[s2] != -INFINITY) wsum += expf(ls[s2] - mx);
-#pragma unroll
-                        for (int s2 = 0; s2 < S; ++s2)
-                            s_f[s2 * kH + h] = wsum > 0.f && ls[s2] != -INFINITY ? expf(ls[s2] - mx) / wsum : 0.f;
-                        if (lse && h % S == sp) lse[c_grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
-                    }
-                    named_bar_sync(1, kSoftmaxThreads);
-                    uint16_t* stage =
-                        reinterpret_cast<uint16_t*>(smem + kOffKV + kStageOff + wl * kStageBytes);
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int dv = 0; dv < 4; ++dv) {
-                        const uint32_t poff = ((uint32_t)dv * kSoftmaxWarps + wl) * kPiece;
-                        uint32_t u[kHPT];
-                        if (nblk > 0) {
-                            tmem_ld_hpt(tmem + lane_base + kTmemO + dv * kH + h0, u);
-                            tmem_ld_wait();
-                        } else {
-#pragma unroll
-                            for (int x = 0; x < kHPT; ++x) u[x] = 0u;
-                        }
-                        uint16_t o16[hq];
-#pragma unroll
-                        for (int j = 0; j < hq; j += 2) {
-                            const int ha = h0 + sp + S * j, hb = ha + S;
-                            // in split order, this rank's term at its place
-                            float acc_a = 0.f, acc_b = 0.f;
-#pragma unroll
-                            for (int s2 = 0; s2 < S; ++s2) {
-                                float va, vb;
-                                if (s2 == sp) {
-                                    // u[sp + S j] with sp < S chosen by selects (no local-memory indexing)
-                                    uint32_t ua = u[S * j], ub = u[S * (j + 1)];
-                                    float ia = inv[S * j], ib = inv[S * (j + 1)];
-#pragma unroll
-                                    for (int q = 1; q < S; ++q)
-                                        if (sp == q) {
-                                            ua = u[S * j + q];
-                                            ub = u[S * (j + 1) + q];
-                                            ia = inv[S * j + q];
-                                            ib = inv[S * (j + 1) + q];
-                                        }
-                                    va = __uint_as_float(ua) * ia;
-                                    vb = __uint_as_float(ub) * ib;
-                                } else {
-                                    const uint32_t w2 = reinterpret_cast<const uint32_t*>(
-                                        smem + kOffQ + s2 * kSlot + poff)[(j / 2) * 32 + lane];
-                                    va = __uint_as_float(w2 << 16);
-                                    vb = __uint_as_float(w2 & 0xFFFF0000u);
-                                }
-                                acc_a = fmaf(s_f[s2 * kH + ha], va, acc_a);
-                                acc_b = fmaf(s_f[s2 * kH + hb], vb, acc_b);
-                            }
-                            const __nv_bfloat16 ba = __float2bfloat16_rn(acc_a), bb = __float2bfloat16_rn(acc_b);
-                            o16[j] = *reinterpret_cast<const uint16_t*>(&ba);
-                            o16[j + 1] = *reinterpret_cast<const uint16_t*>(&bb);
-                        }
-                        store_warp_tile(stage, o16, out + (c_grow * kH + h0 + sp) * kDV + dv * 128 + (int)(lq * 32),
-                                        (int64_t)S * kDV, lane);
-                    }
-                }
-            }
+            if (ok && had_item)
+                cluster_merge_tail<kMode>(smem, tmem, c_sp, c_nblk, (gb - 1u) & 1u, c_grow, out, lse, status);
         }
     }
 
