@@ -187,10 +187,10 @@ DSA_API dsa_status dsa_sparse_mla_fwd(const dsa_batch* batch, const uint16_t* q,
  *                  reported.
  * Returns DSA_ERR_WORKSPACE, before launching anything, when the call's
  * partials would not fit in the 32 MiB array: each partial (one split of one
- * query row) takes 131,328 bytes, so at most 255 fit.  Rows split 2 or 4
+ * query row) takes 131,328 bytes, so at most 255 fit.  Rows split 2, 4 or 8
  * ways merge inside a CTA cluster and need no partials (64 decode rows at
- * k = 2048); 8 rows x 16 splits take 16.8 MB; 100 rows x 3 splits (k = 2047)
- * do not fit.
+ * k = 2048, 8 rows at k = 2048); 40 rows x 3 splits (k = 2048) take 15.8 MB;
+ * 100 rows x 3 splits (k = 2047) do not fit.
  * The first call on a device looks up the array's device address (once per
  * device); make that first call before any stream capture.  The address
  * stays cached for the process: after cudaDeviceReset this call must not be

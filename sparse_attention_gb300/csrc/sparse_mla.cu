@@ -36,11 +36,11 @@
 //               a split's fp32 partial), one column per thread
 // A single 144 KiB row tile fits next to Q (72 KiB); it is refilled chunk
 // by chunk as soon as the MMAs that read each chunk have completed.
-// Split-K partials (for few query rows): with 2 or 4 splits the CTAs of a
-// row form a cluster; each rank merges a share of the heads from its own
-// TMEM and the other ranks' weighted contributions, which arrive by one
-// bulk copy per peer (no scratch memory).  More splits write fp32 partials
-// that merge_kernel combines.
+// Split-K partials (for few query rows): with 2, 4 or 8 splits the CTAs of
+// a row form a cluster; each rank merges a share of the heads from its own
+// TMEM and the other ranks' normalised outputs, which arrive by bulk copies
+// into its shared memory (no scratch memory).  Other split counts write
+// fp32 partials that merge_kernel combines.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -85,7 +85,7 @@ __device__ __forceinline__ void tmem_ld_hpt(uint32_t taddr, uint32_t (&r)[32]) {
 }
 constexpr int64_t kL2PrefetchBytes = int64_t(128) << 20;  // cache bytes above which rows are prefetched
 constexpr int kPrefetchAhead = 1;                         // blocks prefetched ahead of the gather
-constexpr int kMaxClusterMerge = 4;                       // most splits merged inside a cluster
+constexpr int kMaxClusterMerge = 8;                       // most splits merged inside a cluster (portable size)
 constexpr float kRescaleLog2 = 8.0f;         // rescale O only when a max grows by > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -119,7 +119,7 @@ constexpr int kBarRecvLse = kBarPeerFree + 1;                  // cluster merge:
 constexpr int kNumBars = kBarRecvLse + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-// Cluster merge of a row's S = 2 or 4 splits (cluster rank = split).  A
+// Cluster merge of a row's S = 2, 4 or 8 splits (cluster rank = split).  A
 // piece is what one softmax warp sends one peer for one 128-column block dv
 // of O: the peer's kHPT / S heads of the warp's head group at the warp's 32
 // columns, bf16 pairs of heads [j / 2][lane][j % 2], (32 / S) x 64 bytes.
@@ -185,7 +185,7 @@ __device__ __forceinline__ void store_warp_tile(T* stage, const T (&v)[NX], T* d
     __syncwarp();
 }
 
-// The merge of a row's S = 2 or 4 splits inside their cluster (rank =
+// The merge of a row's S = 2, 4 or 8 splits inside their cluster (rank =
 // split), run by the softmax warps of every rank once the split's l and lse
 // (s_l) and its output O^T (TMEM) are final.  Rank sp writes the heads
 // h = sp (mod S):
@@ -367,8 +367,9 @@ __device__ __forceinline__ void cluster_merge_tail(uint8_t* smem, const uint32_t
 enum OutMode : int {
     kOutRows = 0,        // one split per row: bf16 output rows (and lse)
     kOutPartials = 1,    // fp32 split partials, merged by merge_kernel
-    kOutCluster2 = 2,    // the row's 2 or 4 splits merge inside a cluster
+    kOutCluster2 = 2,    // the row's 2, 4 or 8 splits merge inside a cluster
     kOutCluster4 = 4,
+    kOutCluster8 = 8,
 };
 
 template <int kMode>
@@ -1115,9 +1116,17 @@ __global__ void __launch_bounds__(256)
     if (lse && (threadIdx.x & 31) == 0) lse[grow * kH + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
+// Splits merged inside a cluster: the count divides the heads and is small
+// enough that a cluster of that many one-SM CTAs always fits in a GPC.
+bool merge_in_cluster(int splits) { return splits > 1 && splits <= kMaxClusterMerge && kH % splits == 0; }
+
 // CTAs per query row.  One CTA fills an SM's shared memory, so the grid
 // runs in waves of num_sms() CTAs; pick the split count that minimises
-// waves x (blocks per CTA + one block's worth of per-CTA overhead).
+// waves x (blocks per CTA + one block's worth of per-CTA overhead), plus
+// one block for splits that merge through fp32 partials and a second
+// launch rather than inside a cluster (8 x 202,752 decode: 8 cluster
+// splits 24.0 us, 27.3 us from a cold L2, against 24.6 / 31.4 us for 16
+// splits and partials).
 int choose_splits(int64_t rows, int k) {
     if (rows <= 0) return 1;
     const int nblk = std::max(1, (k + kBlk - 1) / kBlk);
@@ -1126,7 +1135,7 @@ int choose_splits(int64_t rows, int k) {
     int64_t best_cost = -1;
     for (int sp = 1; sp <= std::min(16, nblk); ++sp) {
         const int64_t waves = (rows * sp + nsm - 1) / nsm;
-        const int64_t cost = waves * ((nblk + sp - 1) / sp + 1);
+        const int64_t cost = waves * ((nblk + sp - 1) / sp + 1) + (sp > 1 && !merge_in_cluster(sp) ? 1 : 0);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = sp;
@@ -1134,10 +1143,6 @@ int choose_splits(int64_t rows, int k) {
     }
     return best;
 }
-
-// Splits merged inside a cluster: the count divides the heads and is small
-// enough that a cluster of that many one-SM CTAs always fits in a GPC.
-bool merge_in_cluster(int splits) { return splits > 1 && splits <= kMaxClusterMerge && kH % splits == 0; }
 
 }  // namespace
 
@@ -1174,7 +1179,8 @@ cudaError_t launch_sparse_mla(const BatchDev& bd, RowRange rr, const uint16_t* q
     auto* kern = mode == kOutRows       ? sparse_mla_tc_kernel<kOutRows>
                  : mode == kOutPartials ? sparse_mla_tc_kernel<kOutPartials>
                  : mode == kOutCluster2 ? sparse_mla_tc_kernel<kOutCluster2>
-                                        : sparse_mla_tc_kernel<kOutCluster4>;
+                 : mode == kOutCluster4 ? sparse_mla_tc_kernel<kOutCluster4>
+                                        : sparse_mla_tc_kernel<kOutCluster8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     // caches larger than a fraction of L2 are read from HBM: prefetch one

@@ -280,11 +280,12 @@ def test_maximum_batch_of_sequences():
     check_attention(st, idx, out, lse)
 
 
-@pytest.mark.parametrize("B,k", [(64, 256), (38, 512), (19, 1024)])
+@pytest.mark.parametrize("B,k", [(64, 256), (38, 512), (19, 1024), (40, 2048)])
 def test_split_partials_merge(B, k):
-    # decode rows whose selected lists are split over 2 and 4 CTAs (merged
-    # inside a cluster) and 8 CTAs (merged by a second kernel); short
-    # contexts leave the later splits of a row without any valid index
+    # decode rows whose selected lists are split over 2, 4 and 8 CTAs
+    # (merged inside a cluster) and over 3 CTAs (fp32 partials merged by a
+    # second kernel); short contexts leave the later splits of a row
+    # without any valid index
     rng = np.random.default_rng(B)
     ctx = [int(c) for c in rng.integers(2, 3 * k, B)]
     ctx[0], ctx[1] = 1, k // 3
