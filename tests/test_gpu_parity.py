@@ -162,6 +162,38 @@ def test_attention_holes_and_single_index():
     assert np.allclose(out[0].float().cpu().numpy(), np.tile(v, (64, 1)), atol=1e-2, rtol=1e-2)
 
 
+def test_attention_items_of_mixed_block_counts():
+    # 400 query rows over 152 persistent CTAs: each CTA walks two or three
+    # rows whose block counts differ (no valid index, one index, an empty
+    # first block, full and holed selections), so the per-item handshakes
+    # and the read-out of one row overlapping the next row's gathers are
+    # exercised with every shape
+    k = 256
+    bt = W.make_batch_np([600], [400], k=k, seed=80)
+    st = Staged(bt)
+    rng = np.random.default_rng(3)
+    idx = np.full((400, k), -1, dtype=np.int32)
+    for i in range(400):
+        t = 600 - 400 + i                                  # the row's position
+        kind = i % 5
+        if kind == 1:
+            idx[i, 0] = int(rng.integers(0, t + 1))
+        elif kind == 2:                                     # only the second block
+            idx[i, 128:128 + 40] = np.sort(rng.choice(t + 1, size=40, replace=False))
+        elif kind == 3:                                     # every position it may see, up to k
+            n = min(k, t + 1)
+            idx[i, :n] = np.sort(rng.choice(t + 1, size=n, replace=False))
+        elif kind == 4:
+            idx[i, ::2] = np.sort(rng.choice(t + 1, size=k // 2, replace=False))
+    ix = torch.from_numpy(idx).cuda()
+    out, lse = st.attention(ix)
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    empty = torch.from_numpy(np.arange(400) % 5 == 0).cuda()
+    assert torch.all(out[empty].float() == 0) and torch.all(torch.isneginf(lse[empty]))
+    check_attention(st, ix, out, lse)
+
+
 def test_attention_empty_selection_and_bad_index():
     bt = W.make_batch_np([50], [2], k=8, seed=78)
     st = Staged(bt)
@@ -280,12 +312,13 @@ def test_maximum_batch_of_sequences():
     check_attention(st, idx, out, lse)
 
 
-@pytest.mark.parametrize("B,k", [(64, 256), (38, 512), (19, 1024), (40, 2048)])
+@pytest.mark.parametrize("B,k", [(64, 256), (38, 512), (19, 1024), (40, 2048), (100, 2048)])
 def test_split_partials_merge(B, k):
     # decode rows whose selected lists are split over 2, 4 and 8 CTAs
     # (merged inside a cluster) and over 3 CTAs (fp32 partials merged by a
-    # second kernel); short contexts leave the later splits of a row
-    # without any valid index
+    # second kernel; at 100 rows a persistent CTA walks two of the 300
+    # items); short contexts leave the later splits of a row without any
+    # valid index
     rng = np.random.default_rng(B)
     ctx = [int(c) for c in rng.integers(2, 3 * k, B)]
     ctx[0], ctx[1] = 1, k // 3
