@@ -125,6 +125,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// The same with an L2 eviction policy for the line read (createpolicy).
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+                 : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the arrival is counted in the barrier's expected count).
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
