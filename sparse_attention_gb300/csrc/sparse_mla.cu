@@ -9,7 +9,9 @@
 // is one stream shared by all heads; section 2.5: 576-wide cached rows; the
 // GLM-5 explainer page: the top-2048 ids only drive the gather.)
 //
-// One CTA per (query row, segment of its selected list).  With only 64
+// Work items are (query row, segment of its selected list); a CTA walks
+// items blockIdx.x, + gridDim.x, ... (one persistent CTA per SM), or holds
+// one item when a row's segments merge in a cluster.  With only 64
 // heads, a heads-as-M MMA would run at M = 64, half the tensor rate; so the
 // products are taken transposed, with the 128 gathered rows of a block on
 // the M = 128 side:
@@ -20,11 +22,14 @@
 //   warps 0, 1  producers: validate the block's indices and gather the
 //               576-wide rows with 16-byte cp.async copies (8 lanes per
 //               128-byte row piece, coalesced; 8 rows per instruction pair)
-//               into nine 64-column chunks laid out 128B-swizzled.  When
-//               the caches do not stay in L2, the rows of the next block are
-//               prefetched into L2 (the first block's during the index
-//               scan), so that a gather waits on L2 rather than on HBM
-//   warp 2      TMEM owner; loads Q once by TMA; MMA issuer
+//               into nine 64-column chunks laid out 128B-swizzled; they
+//               scan an item's indices (one round trip) and publish its
+//               block count.  When the caches do not stay in L2, the rows
+//               of the next block are prefetched into L2 (the first two
+//               blocks' during the scan), so that a gather waits on L2
+//               rather than on HBM, and split items gather with an
+//               evict-first policy (each row is read once)
+//   warp 2      TMEM owner; loads each item's Q by TMA; MMA issuer
 //   warps 3..10 softmax: thread = one gathered row and 32 of the heads (two
 //               warps per TMEM lane quarter).  The running per-head max m
 //               only moves when some score exceeds it by more than 2^8 (a
@@ -33,7 +38,12 @@
 //               and O^T rescaled in TMEM.  p = 2^(s*c - m) in fp32, written
 //               as bf16 P^T over the RoPE chunk (free once S^T is done);
 //               final normalisation straight from TMEM into the output (or
-//               a split's fp32 partial), one column per thread
+//               a split's fp32 partial), one column per thread.  A CTA's
+//               first item starts with a side-effect-free pass over the
+//               block code while the first tile is in flight (the code is
+//               otherwise fetched cold)
+// Behind a top-k launch (programmatic dependent launch), a CTA sets itself
+// up before the dependency wait, which only the producers take.
 // A single 144 KiB row tile fits next to Q (72 KiB); it is refilled chunk
 // by chunk as soon as the MMAs that read each chunk have completed.
 // Split-K partials (for few query rows): with 2, 4 or 8 splits the CTAs of
