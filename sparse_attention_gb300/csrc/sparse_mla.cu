@@ -521,8 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // loads when the rows are 16-byte aligned, one round trip); with
             // L2 prefetching on, the rows of the first 1 + kPrefetchAhead
             // blocks are prefetched as their indices are seen
+            // (in the split instances the softmax warps prefetch the first
+            // item's rows: they are idle then, and the scan reaches its first
+            // gathers sooner)
             auto prefetch_row = [&](int j, int32_t sv) {
-                if (l2_prefetch && j < I.j_begin + (1 + kPrefetchAhead) * kBlk && sv >= 0 && sv <= I.t)
+                if (l2_prefetch && (kMode == kOutRows || nitem > 0) && j < I.j_begin + (1 + kPrefetchAhead) * kBlk &&
+                    sv >= 0 && sv <= I.t)
                     prefetch_l2_bulk(kv_seq + (int64_t)sv * (kDQK * 2), kDQK * 2);
             };
             int last = -1;
@@ -985,6 +989,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s_thr[st] = -INFINITY;
                     }
                     named_bar_sync(1, kSoftmaxThreads);
+                    if (kMode != kOutRows && l2_prefetch) {
+                        // the rows of the first item's first 1 + kPrefetchAhead
+                        // blocks (one index per thread; these warps are idle
+                        // until the first S^T tile; the row instance keeps
+                        // them in the producers' scan, its code unchanged)
+                        pdl_wait();      // the indices of the previous launch are complete
+                        const uint8_t* kv_seq =
+                            reinterpret_cast<const uint8_t*>(kv) + (int64_t)I.b * bd.stride * (kDQK * 2);
+                        for (int j = I.j_begin + st; j < min(I.j_end, I.j_begin + (1 + kPrefetchAhead) * kBlk);
+                             j += kSoftmaxThreads) {
+                            const int32_t sv = __ldg(I.sel + j);
+                            if (sv >= 0 && sv <= I.t) prefetch_l2_bulk(kv_seq + (int64_t)sv * (kDQK * 2), kDQK * 2);
+                        }
+                    }
                     continue;
                 }
                 if (lane == 0) mbar_arrive(bar(kBarP));
