@@ -86,6 +86,7 @@ struct alignas(16) TopkSmem {
     int32_t cand_pos[kMaxCand];
     uint32_t warp_sums[32];
     uint32_t wcnt[32], wgt[32], weq[32], wmax[32];
+    uint32_t group[kBins / 32];           // this CTA's counts of 64 groups of 32 bins (cluster selects)
     uint32_t small[64];                   // this CTA's keys of a small boundary bin
     uint32_t small_all[64];               // the bin's keys of the whole cluster
     uint32_t total, sel_digit, sel_above, sel_count, chunk_total;
@@ -119,59 +120,115 @@ __device__ uint32_t radix_select(cg::cluster_group& cluster, int nranks, TopkSme
         visit([&](uint32_t key) {
             if ((key & pmask) == prefix) atomicAdd(&S.hist[(key >> sh) & dmask], 1u);
         });
-        // thread tid owns bins [4 tid, 4 tid + 4), summed over the ranks
-        uint32_t c[kBinsPerThread];
-        uint32_t mine = 0u;
-        if (nranks == 1) {
+        if (nranks > 1) {
+            // Over a cluster: the group of 32 bins that holds the need-th
+            // largest key, from every rank's 64 group counts, then its bin
+            // from every rank's 32 counts of that group (the bin the flat
+            // scan below would find, from 3 % of the remote reads).
+            constexpr int kGroups = kBins / 32;
+            __syncthreads();                           // this rank's histogram is complete
+            if (tid < kGroups) {
+                uint32_t g = 0u;
+#pragma unroll 8
+                for (int b2 = 0; b2 < 32; ++b2) g += S.hist[32 * tid + b2];
+                S.group[tid] = g;
+            }
+            cluster.sync();                            // every rank's group counts are ready
+            if (warp == 0) {
+                // lane l: groups 2l and 2l + 1, summed over the ranks in rank order
+                uint32_t g0 = 0u, g1 = 0u;
+                {
+                    uint32_t r0[kMaxCluster], r1[kMaxCluster];
+#pragma unroll
+                    for (int r = 0; r < kMaxCluster; ++r) {
+                        const uint32_t* h = cluster.map_shared_rank(S.group, (unsigned)min(r, nranks - 1));
+                        r0[r] = r < nranks ? h[2 * lane] : 0u;
+                        r1[r] = r < nranks ? h[2 * lane + 1] : 0u;
+                    }
+#pragma unroll
+                    for (int r = 0; r < kMaxCluster; ++r) {
+                        g0 += r0[r];
+                        g1 += r1[r];
+                    }
+                }
+                const uint32_t incl = warp_inclusive_scan(g0 + g1);
+                const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+                const uint32_t above1 = total - incl;  // keys in groups above 2l + 1
+                const uint32_t above0 = above1 + g1;   // keys in groups above 2l
+                int grp = -1;
+                uint32_t gabove = 0u;
+                if (above1 < need && need <= above1 + g1) {
+                    grp = 2 * (int)lane + 1;
+                    gabove = above1;
+                } else if (above0 < need && need <= above0 + g0) {
+                    grp = 2 * (int)lane;
+                    gabove = above0;
+                }
+                const uint32_t has = __ballot_sync(0xffffffffu, grp >= 0);
+                const int src = has ? __ffs(has) - 1 : 0;
+                grp = __shfl_sync(0xffffffffu, grp, src);
+                gabove = __shfl_sync(0xffffffffu, gabove, src);
+                if (has) {
+                    // lane l: bin 32 grp + l, summed over the ranks in rank order
+                    uint32_t rb[kMaxCluster];
+#pragma unroll
+                    for (int r = 0; r < kMaxCluster; ++r) {
+                        const uint32_t* h = cluster.map_shared_rank(S.hist, (unsigned)min(r, nranks - 1));
+                        rb[r] = r < nranks ? h[32 * grp + lane] : 0u;
+                    }
+                    uint32_t cb = 0u;
+#pragma unroll
+                    for (int r = 0; r < kMaxCluster; ++r) cb += rb[r];
+                    const uint32_t bincl = warp_inclusive_scan(cb);
+                    const uint32_t gtot = __shfl_sync(0xffffffffu, bincl, 31);
+                    const uint32_t above = gabove + (gtot - bincl);   // keys in higher bins
+                    if (above < need && need <= above + cb) {
+                        S.sel_digit = (uint32_t)(32 * grp + (int)lane);
+                        S.sel_above = above;
+                        S.sel_count = cb;
+                    }
+                }
+                if (lane == 0) S.total = total;
+            }
+            cluster.sync();                            // every remote read done before any bin is cleared
+#pragma unroll
+            for (int x = 0; x < kBinsPerThread; ++x) S.hist[kBinsPerThread * tid + x] = 0u;
+            __syncthreads();
+        } else {
+            // thread tid owns bins [kBinsPerThread tid, kBinsPerThread (tid + 1))
+            uint32_t c[kBinsPerThread];
+            uint32_t mine = 0u;
             __syncthreads();
 #pragma unroll
             for (int x = 0; x < kBinsPerThread; ++x) c[x] = S.hist[kBinsPerThread * tid + x];
-        } else {
-            cluster.sync();
-            // every rank's counts loaded at once (predicated loads, one
-            // distributed-shared-memory round trip), then summed in rank order
-            uint32_t rc[kMaxCluster][kBinsPerThread];
-#pragma unroll
-            for (int r = 0; r < kMaxCluster; ++r) {
-                const uint32_t* h = cluster.map_shared_rank(S.hist, (unsigned)min(r, nranks - 1));
-#pragma unroll
-                for (int x = 0; x < kBinsPerThread; ++x) rc[r][x] = r < nranks ? h[kBinsPerThread * tid + x] : 0u;
-            }
 #pragma unroll
             for (int x = 0; x < kBinsPerThread; ++x) {
-                c[x] = 0u;
-#pragma unroll
-                for (int r = 0; r < kMaxCluster; ++r) c[x] += rc[r][x];
+                S.hist[kBinsPerThread * tid + x] = 0u;
+                mine += c[x];
             }
-            cluster.sync();                        // every remote read done before any bin is cleared
-        }
-#pragma unroll
-        for (int x = 0; x < kBinsPerThread; ++x) {
-            S.hist[kBinsPerThread * tid + x] = 0u;
-            mine += c[x];
-        }
-        // keys in higher bins = total - inclusive scan in bin order
-        const uint32_t incl_w = warp_inclusive_scan(mine);
-        if (lane == 31) S.warp_sums[warp] = incl_w;
-        __syncthreads();
-        if (warp == 0) {
-            const uint32_t v = lane < kWarps ? S.warp_sums[lane] : 0u;
-            const uint32_t sc = warp_inclusive_scan(v);
-            if (lane < kWarps) S.warp_sums[lane] = sc;
-            if (lane == kWarps - 1) S.total = sc;
-        }
-        __syncthreads();
-        uint32_t above = S.total - (incl_w + (warp ? S.warp_sums[warp - 1] : 0u));
-#pragma unroll
-        for (int x = kBinsPerThread - 1; x >= 0; --x) {
-            if (above < need && need <= above + c[x]) {
-                S.sel_digit = (uint32_t)(kBinsPerThread * tid + x);
-                S.sel_above = above;
-                S.sel_count = c[x];
+            // keys in higher bins = total - inclusive scan in bin order
+            const uint32_t incl_w = warp_inclusive_scan(mine);
+            if (lane == 31) S.warp_sums[warp] = incl_w;
+            __syncthreads();
+            if (warp == 0) {
+                const uint32_t v = lane < kWarps ? S.warp_sums[lane] : 0u;
+                const uint32_t sc = warp_inclusive_scan(v);
+                if (lane < kWarps) S.warp_sums[lane] = sc;
+                if (lane == kWarps - 1) S.total = sc;
             }
-            above += c[x];
+            __syncthreads();
+            uint32_t above = S.total - (incl_w + (warp ? S.warp_sums[warp - 1] : 0u));
+#pragma unroll
+            for (int x = kBinsPerThread - 1; x >= 0; --x) {
+                if (above < need && need <= above + c[x]) {
+                    S.sel_digit = (uint32_t)(kBinsPerThread * tid + x);
+                    S.sel_above = above;
+                    S.sel_count = c[x];
+                }
+                above += c[x];
+            }
+            __syncthreads();
         }
-        __syncthreads();
         need -= S.sel_above;
         prefix |= S.sel_digit << sh;
         pmask |= dmask << sh;
