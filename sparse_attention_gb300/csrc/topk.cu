@@ -415,8 +415,8 @@ __global__ void __launch_bounds__(NT, NT <= 512 ? 2 : 1)
     // Keys are tested as floats against the float of L (the same order as
     // the keys, -0.0 == +0.0).  The per-group candidate counts of a lane
     // travel through one 64-bit warp scan (8-bit fields), which places every
-    // candidate of the step in position order; candidates are re-read (L1
-    // hits) to be converted and stored.
+    // candidate of the step in position order; their keys are read again
+    // after the pass.
     const int32_t seg = ((s_hi - s_lo + kWarps - 1) / kWarps + 127) & ~127;
     const int32_t w_lo = min(s_hi, s_lo + warp * seg), w_hi = min(s_hi, w_lo + seg);
     uint32_t* rk = S.cand_key + warp * kRegion;
@@ -465,15 +465,22 @@ __global__ void __launch_bounds__(NT, NT <= 512 ? 2 : 1)
             uint32_t at = base + ((uint32_t)((incl - packed) >> (8 * u)) & 0xFFu);
             for (uint32_t bb = (bits >> (4 * u)) & 0xFu; bb; bb &= bb - 1u) {
                 const int32_t j = jb + 128 * u + 4 * (int32_t)lane + (int32_t)(__ffs(bb) - 1);
-                if (at < (uint32_t)kRegion) {
-                    rk[at] = row_key(j);
-                    rp[at] = j;
-                }
+                if (at < (uint32_t)kRegion) rp[at] = j;
                 ++at;
             }
             base += (uint32_t)(tot >> (8 * u)) & 0xFFu;
         }
         cnt = base;
+    }
+    // the candidates' keys, re-read (L1 or L2 hits) once the pass is done:
+    // independent loads, many in flight (reading each as it was appended put
+    // one round trip per candidate on the pass: 7 K of its ~12 K cycles in a
+    // decode row)
+    __syncwarp();
+    {
+        const uint32_t n = min(cnt, (uint32_t)kRegion);
+#pragma unroll 4
+        for (uint32_t s = lane; s < n; s += 32) rk[s] = row_key(rp[s]);
     }
     // an upper bound of the candidates (keys of the slice, -inf when empty)
     uint32_t cmax = fmx >= Lf ? order_key(fmx) : 0u;
