@@ -92,6 +92,7 @@ struct alignas(16) TopkSmem {
     uint32_t total, sel_digit, sel_above, sel_count, chunk_total;
     uint32_t small_n, small_all_n, small_tau, small_need;
     uint32_t cta_cand, cta_overflow, cta_gt, cta_eq, cta_max;   // read by the rest of the cluster
+    uint32_t all_cand, all_overflow, all_max, pre_gt, pre_eq;    // the cluster's, combined by warp 0
 };
 
 // The k-th largest of the keys that `visit` hands to this thread's callback,
@@ -313,21 +314,25 @@ __device__ __forceinline__ int varying_bits(uint32_t lo, uint32_t hi) {
 template <int NT>
 __device__ __forceinline__ void cluster_prefix(cg::cluster_group& cluster, int crank, TopkSmem<NT>& S,
                                                uint32_t& gt0, uint32_t& eq0) {
-    // every lower rank's counts loaded at once (predicated), then summed
-    uint32_t g[kMaxCluster], e[kMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {
+    // lane r of warp 0 loads lower rank r's counts (one remote read per
+    // rank, not one per thread), the warp sums them, the CTA shares them
+    if ((threadIdx.x >> 5) == 0) {
+        const int r = (int)(threadIdx.x & 31);
         const TopkSmem<NT>* o = cluster.map_shared_rank(&S, (unsigned)min(r, max(crank - 1, 0)));
-        g[r] = r < crank ? o->cta_gt : 0u;
-        e[r] = r < crank ? o->cta_eq : 0u;
-    }
-    gt0 = 0u;
-    eq0 = 0u;
+        uint32_t g = r < crank ? o->cta_gt : 0u, e = r < crank ? o->cta_eq : 0u;
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {
-        gt0 += g[r];
-        eq0 += e[r];
+        for (int off = 16; off > 0; off >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, off);
+            e += __shfl_xor_sync(0xffffffffu, e, off);
+        }
+        if (r == 0) {
+            S.pre_gt = g;
+            S.pre_eq = e;
+        }
     }
+    __syncthreads();
+    gt0 = S.pre_gt;
+    eq0 = S.pre_eq;
 }
 
 // out[pos] = v for a rank pos < k; a rank outside the row would be a bug:
@@ -508,21 +513,29 @@ __global__ void __launch_bounds__(NT, NT <= 512 ? 2 : 1)
         any_overflow = S.cta_overflow;
         all_max = S.cta_max;
     } else {
-        // every rank's counts loaded at once (predicated), then combined
-        uint32_t cc[kMaxCluster], co[kMaxCluster], cm[kMaxCluster];
-#pragma unroll
-        for (int q = 0; q < kMaxCluster; ++q) {
+        // lane q of warp 0 loads rank q's counts (one remote read per rank,
+        // not one per thread), the warp combines them, the CTA shares them
+        if (warp == 0) {
+            const int q = lane;
             const TopkSmem<NT>* o = cluster.map_shared_rank(&S, (unsigned)min(q, csize - 1));
-            cc[q] = q < csize ? o->cta_cand : 0u;
-            co[q] = q < csize ? o->cta_overflow : 0u;
-            cm[q] = q < csize ? o->cta_max : 0u;
-        }
+            uint32_t cc = q < csize ? o->cta_cand : 0u, co = q < csize ? o->cta_overflow : 0u,
+                     cm = q < csize ? o->cta_max : 0u;
 #pragma unroll
-        for (int q = 0; q < kMaxCluster; ++q) {
-            all_cand += cc[q];
-            any_overflow |= co[q];
-            all_max = max(all_max, cm[q]);
+            for (int off = 16; off > 0; off >>= 1) {
+                cc += __shfl_xor_sync(0xffffffffu, cc, off);
+                co |= __shfl_xor_sync(0xffffffffu, co, off);
+                cm = max(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+            }
+            if (lane == 0) {
+                S.all_cand = cc;
+                S.all_overflow = co;
+                S.all_max = cm;
+            }
         }
+        __syncthreads();
+        all_cand = S.all_cand;
+        any_overflow = S.all_overflow;
+        all_max = S.all_max;
     }
     const bool use_candidates = !any_overflow && all_cand >= (uint32_t)k;
 
