@@ -23,14 +23,14 @@ namespace {
 constexpr size_t kScoreChunkBytes = size_t(512) << 20;
 
 // Inside dsa_forward the top-k and attention launches of decode-sized
-// batches (fewer query rows than SMs, rows of at most 64 K positions) are
-// programmatic dependents of the launch before them: their CTAs become
-// resident while that kernel drains, and wait for it before reading its
-// results (64 x 32,768 decode step 154.6 -> 151.2 us).  Many-row prefills
-// and cluster-split long rows ran slightly slower chained (7.72 -> 7.74 ms,
-// 120.8 -> 121.7 us), so they launch plainly.
+// batches (fewer query rows than SMs) are programmatic dependents of the
+// launch before them: their CTAs become resident while that kernel drains,
+// and wait for it before reading its results (64 x 32,768 decode step
+// 154.6 -> 151.2 us; 8 x 202,752, whose rows the top-k and the attention
+// split over clusters, 104.8 -> 99.7 us).  Many-row prefills ran slightly
+// slower chained (7.72 -> 7.74 ms), so they launch plainly.
 bool chain_launches(const dsa_batch* b) {
-    return (int64_t)b->batch * b->max_q < num_sms() && b->max_ctx <= 65536;
+    return (int64_t)b->batch * b->max_q < num_sms();
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
