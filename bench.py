@@ -810,6 +810,31 @@ def run_dsa(args):
         dist.destroy_process_group()
 
 
+def pack_layout(srcs, align: int = 256):
+    """Byte layout of tensors packed one after another into one block:
+    {name: (offset, nbytes, dtype, shape)} and the block's size; every
+    offset is a multiple of `align`."""
+    segs, nbytes = {}, 0
+    for n, t in srcs:
+        segs[n] = (nbytes, t.numel() * t.element_size(), t.dtype, t.shape)
+        nbytes = (nbytes + segs[n][1] + align - 1) // align * align
+    return segs, nbytes
+
+
+def pack_into(blk, segs, srcs):
+    """Copies each tensor's bytes to its place in the uint8 block."""
+    import torch
+    for n, t in srcs:
+        o0, nb, _, _ = segs[n]
+        blk[o0:o0 + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+
+
+def seg_view(blk, segs, n):
+    """Tensor n as a view of the block (its dtype and shape)."""
+    o0, nb, dt, shape = segs[n]
+    return blk[o0:o0 + nb].view(dt).view(shape)
+
+
 def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
     """Same metric through the public API with every step's inputs copied in
     from pinned host memory and its result read back to pinned host memory.
@@ -864,21 +889,12 @@ def run_e2e(case: Case, K: int, Wu: int, barrier, max_over_ranks, world: int):
     # are views of that block (256-byte aligned) and the rows are staged in
     # it before being scattered into their cache rows.
     srcs = list(own.items()) + [(f"row:{a}", r.contiguous()) for (_, a, _), r in zip(owners, rows[0])]
-    segs, nbytes = {}, 0
-    for n, t in srcs:
-        segs[n] = (nbytes, t.numel() * t.element_size(), t.dtype, t.shape)
-        nbytes = (nbytes + segs[n][1] + 255) // 256 * 256
+    segs, nbytes = pack_layout(srcs)
     host_blk = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-    for n, t in srcs:
-        o0, nb, _, _ = segs[n]
-        host_blk[o0:o0 + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+    pack_into(host_blk, segs, srcs)
     dev_blk = [torch.empty(nbytes, dtype=torch.uint8, device=comp.device) for _ in range(2)]
-
-    def seg_view(blk, n):
-        o0, nb, dt, shape = segs[n]
-        return blk[o0:o0 + nb].view(dt).view(shape)
-    bufs = [{n: seg_view(dev_blk[k], n) for n in own} for k in range(2)]
-    stage = [[seg_view(dev_blk[k], f"row:{a}") for _, a, _ in owners] for k in range(2)]
+    bufs = [{n: seg_view(dev_blk[k], segs, n) for n in own} for k in range(2)]
+    stage = [[seg_view(dev_blk[k], segs, f"row:{a}") for _, a, _ in owners] for k in range(2)]
     h2d = nbytes
     d2h = out_h[0].numel() * out_h[0].element_size()
     ev_in = [torch.cuda.Event() for _ in range(2)]
