@@ -87,9 +87,9 @@ typedef enum dsa_status {
     DSA_ERR_INTERNAL = 8     /* device: an internal consistency check failed (a bug); the write was skipped */
 } dsa_status;
 
-/* One call's batch.  q_off and ctx_len are DEVICE int32 arrays so that a
- * captured launch sequence can be replayed with new lengths; the host only
- * gives upper bounds, used to size grids.  Device-side requirements, checked
+/* One call's batch.  q_off and ctx_len are DEVICE int32 arrays, read by the
+ * kernels: the lengths may change on the device between calls that keep the
+ * same host arguments; the host only gives upper bounds, used to size grids.  Device-side requirements, checked
  * by the kernels (DSA_ERR_BAD_BATCH): q_off[0] = 0, q_off[batch] = total_q,
  * 0 <= n_b <= max_q, n_b <= ctx_len[b] <= max_ctx. */
 typedef struct dsa_batch {
